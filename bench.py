@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode hot path on one GB300 (or N replicas).
+
+Workload (the configuration the headline metric is quoted on): a
+LLaMA-13B-shaped single layer -- 64 sequences, 40 heads x 128, block size 16,
+context lengths uniform in [128, 2048] (seed 1), fp16 K/V/q ~ N(0, 1), pool
+sized to the blocks in use + 10 %, block placement a seeded random
+permutation.  Synthetic data; no model weights are involved.
+
+One step = the whole decode hot path over the batch:
+  pa_reshape_and_cache  (each sequence's newest token -> its slot)
+  pa_decode             (planning kernel + persistent split-KV decode kernel
+                         with the fused log-sum-exp merge)
+The slot mapping and the block tables come from the host before timing (the
+host allocator is never inside the timed region).
+
+Printed: one JSON line (rank 0).  `value` = algorithmic HBM bytes of the step
+/ step time (GB/s), over all ranks; `seq_steps_per_s` beside it.  K/V bytes
+per step (1.4 GB) are >10x the 129 MB L2, so no L2 flush between steps.
+
+`--impl reference` times the CPU oracle (fp64, plain C, OpenMP) on the same
+workload instead, on the host cores, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and seq-steps/sec"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) per pa_decode call on this workload, from the ncu
+# capture summarised in profiles/; valid only for the decode kernel source
+# whose sha256 prefix is given (otherwise reported as null).
+TRAFFIC = {"bytes_per_launch": None, "kernel_sha256_prefix": None}
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_35_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_bytes(ctx_lens, H, D, B, elt) -> int:
+    """Algorithmic bytes of one pa_decode call: K and V of every context
+    token, q and out rows, the table entries covering the contexts, and the
+    context lengths."""
+    kv = 2 * sum(int(c) for c in ctx_lens) * H * D * elt
+    qo = 2 * len(ctx_lens) * H * D * elt
+    tables = 4 * sum(-(-int(c) // B) for c in ctx_lens)
+    return kv + qo + tables + 4 * len(ctx_lens)
+
+
+def scatter_bytes(T, H, D, elt) -> int:
+    """pa_reshape_and_cache: read k_new, v_new, write their slots, read slots."""
+    return 4 * T * H * D * elt + 8 * T
+
+
+def kv_bytes_per_token(layers, heads, head_dim, elt) -> int:
+    """K and V bytes one token occupies in a model of `layers` layers."""
+    return 2 * layers * heads * head_dim * elt
+
+
+# ---- clocks ---------------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:
+            inside = [s for _, s in self.samples]
+            window = "whole run (timed region shorter than the sampling period)"
+        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            for n, v in zip(names, s[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        pw = [float(s[3]) for s in inside if s[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "power_w_max": max(pw) if pw else None, "samples": len(inside),
+                "window": window}
+
+
+# ---- distributed plumbing ------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, world, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---- workload ---------------------------------------------------------------------------------------
+def workload_config(w, NB):
+    return {"workload": "llama13b_decode_b64: 64 seqs x 40 heads x 128, block 16, ctx U[128,2048], fp16",
+            "num_seqs": w.num_seqs, "num_heads": w.num_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "pool_blocks": NB, "context_lens": "uniform [128, 2048], seed 1", "kv_dtype": "fp16",
+            "placement": "seeded random permutation of the pool",
+            "step": "pa_reshape_and_cache (1 new token/seq) + pa_decode over ctx",
+            "l2": "no flush: K/V read per step (~1.4 GB) >> 129 MB L2"}
+
+
+def cpu_oracle_time(w, host, budget_s: float, max_reps: int = 1000):
+    """Time the oracle (scatter + decode) on the whole workload, repeated
+    until ~budget_s.  Returns (seconds per rep, reps, threads)."""
+    import numpy as np
+
+    import oracle
+
+    kb0, vb0 = oracle.pool_bits(host["k_pool"]), oracle.pool_bits(host["v_pool"])
+    tb = w.block_tables.numpy()
+    slots = np.array([oracle.slot_of(tb[s], int(w.new_pos[s]), w.block_size) for s in range(w.num_seqs)],
+                     dtype=np.int64)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.reshape_and_cache(host["k_new"], host["v_new"], kb0, vb0, slots, w.block_size)
+        oracle.decode(host["q"], kb0, vb0, w.block_tables, w.context_lens, w.block_size, w.scale, "f16")
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            return el / reps, reps, oracle.num_threads()
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: rank 0 only."""
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    import pa_workloads as W
+
+    oracle.build()
+    w = W.llama13b_decode(device="cpu")
+    host = {k: getattr(w, k) for k in ("k_pool", "v_pool", "q", "k_new", "v_new")}
+    elt = 2
+    step_b = decode_bytes(w.context_lens.tolist(), w.num_heads, w.head_dim, w.block_size, elt) + scatter_bytes(
+        w.num_seqs, w.num_heads, w.head_dim, elt)
+    # warm-up reps (untimed), then K timed steps; each step is the whole
+    # workload unless that would exceed ~60 s in total, in which case each
+    # step runs on a fixed subset of the sequences.
+    t_one, _, thr = cpu_oracle_time(w, host, 0.0, 1)
+    for _ in range(max(0, args.warmup - 1)):
+        cpu_oracle_time(w, host, 0.0, 1)
+    frac = min(1.0, 60.0 / max(1e-9, t_one * args.steps))
+    nsub = max(1, int(w.num_seqs * frac))
+    sub = W.DecodeWorkload(**{**w.__dict__})
+    idx = torch.arange(nsub)
+    sub.context_lens, sub.new_pos = w.context_lens[idx], w.new_pos[idx]
+    sub.block_tables = w.block_tables[idx]
+    sub_host = {"k_pool": host["k_pool"], "v_pool": host["v_pool"], "q": host["q"][idx], "k_new": host["k_new"][idx],
+                "v_new": host["v_new"][idx]}
+    sub_b = decode_bytes(sub.context_lens.tolist(), w.num_heads, w.head_dim, w.block_size, elt) + scatter_bytes(
+        nsub, w.num_heads, w.head_dim, elt)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_oracle_time(sub, sub_host, 0.0, 1)
+    el = time.perf_counter() - t0
+    gbs = sub_b * args.steps / el / 1e9
+    sample = (f"{nsub} of {w.num_seqs} sequences x {w.num_heads} heads per step" if nsub < w.num_seqs
+              else "whole workload per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, w.num_blocks),
+        "seq_steps_per_s": nsub * args.steps / el,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "step_bytes_full_workload": step_b,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_35_gb300 as pa
+    import pa_workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.llama13b_decode(device=dev)
+    S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
+    elt = 2
+    slots = pa.pa_slot_mapping(w.block_tables, np.arange(S), w.new_pos, B)
+    slots_d = torch.from_numpy(slots).to(dev)
+    tables_d = w.block_tables.to(dev)
+    ctx_d = w.context_lens.to(dev)
+    mx = int(w.context_lens.max())
+    out = torch.empty(S, H, D, dtype=torch.float16, device=dev)
+    ws = pa.decode_workspace(S, H, D, mx, device=dev)
+    err = pa.new_error_flag(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.pa_reshape_and_cache(w.k_new, w.v_new, w.k_pool, w.v_pool, slots_d, err, stream)
+        pa.pa_decode(out, w.q, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    flags = pa.pa_get_error(err, stream)
+    if flags:
+        raise RuntimeError(f"device error flags {flags} during warm-up")
+
+    dbytes = decode_bytes(w.context_lens.tolist(), H, D, B, elt)
+    sbytes = scatter_bytes(S, H, D, elt)
+    step_b = dbytes + sbytes
+
+    # ---- device-timed region
+    K = args.steps
+    dec_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    dec_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    h0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        pa.pa_reshape_and_cache(w.k_new, w.v_new, w.k_pool, w.v_pool, slots_d, err, stream)
+        dec_s[i].record(stream)
+        pa.pa_decode(out, w.q, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err, stream=stream)
+        dec_e[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    h1 = time.time()
+    dist_barrier(world)
+    clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in zip(dec_s, dec_e)]
+    flags = pa.pa_get_error(err, stream)
+    if flags:
+        raise RuntimeError(f"device error flags {flags} in the timed region")
+    max_ms = dist_max(total_ms, world)
+    total_s = max_ms / 1e3
+    value = step_b * K * world / total_s / 1e9
+    seq_steps = S * K * world / total_s
+
+    # ---- end to end through the API: pinned host inputs in, result out, every step
+    Ke = min(K, 200)
+    pin = lambda t: t.detach().cpu().pin_memory()
+    h_q, h_k, h_v = pin(w.q), pin(w.k_new), pin(w.v_new)
+    h_slots, h_tables, h_ctx = pin(torch.from_numpy(slots)), pin(w.block_tables), pin(w.context_lens)
+    h_out = torch.empty(S, H, D, dtype=torch.float16).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(w.q), torch.empty_like(w.k_new), torch.empty_like(w.v_new)
+    d_slots, d_tables, d_ctx = torch.empty_like(slots_d), torch.empty_like(tables_d), torch.empty_like(ctx_d)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tables, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_tables, h_tables), (d_ctx, h_ctx)):
+            d.copy_(h, non_blocking=True)
+        pa.pa_reshape_and_cache(d_k, d_v, w.k_pool, w.v_pool, d_slots, err, stream)
+        pa.pa_decode(out, d_q, w.k_pool, w.v_pool, d_tables, d_ctx, mx, w.scale, ws, err, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    dist_barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist_max(e0.elapsed_time(e1), world)
+    e2e_value = step_b * Ke * world / (e2e_ms / 1e3) / 1e9
+
+    peak, peak_kind = load_peaks()
+    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    achieved = dbytes / dec_avg_s / 1e9
+    sha = kernel_sha()
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha256_prefix"] == sha else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic", "config": {**workload_config(w, w.num_blocks), "parallelism": f"replicas x{world}"},
+        "seq_steps_per_s": seq_steps,
+        "hbm_frac_of_measured_peak": value / world / peak,
+        "hbm_frac_of_nominal_8tbs": value / world / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "kernel": "pa_decode call (planning kernel + persistent decode kernel)",
+                     "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": dec_avg_s * 1e3,
+                     "kernel_sha256_prefix": sha},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / Ke, "steps": Ke},
+        "gpu_launches": 3 * K,
+        "clocks": clocks.summary(h0, h1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        host = {k: getattr(w, k).cpu() for k in ("k_pool", "v_pool", "q", "k_new", "v_new")}
+        wc = W.DecodeWorkload(**{**w.__dict__})
+        t_rep, reps, thr = cpu_oracle_time(wc, host, args.cpu_budget)
+        line["cpu_baseline"] = {"value": step_b / t_rep / 1e9, "unit": "GB/s", "cores": thr, "kind": "oracle",
+                                "sample": f"whole workload (scatter + decode), {reps} repetitions, "
+                                          f"{t_rep * reps:.1f} s wall"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU-oracle timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    rank, world, local = dist_setup()
+    run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

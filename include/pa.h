@@ -1,0 +1,244 @@
+/*
+ * pa.h -- C ABI of libpa: paged KV-cache attention for one NVIDIA GB300
+ * (sm_103a).
+ *
+ * Sources of the operations (the method is PagedAttention, "Efficient
+ * Memory Management for Large Language Model Serving with PagedAttention";
+ * three pages describe it):
+ *   [summary]  paper-summary page of that title (urban-dandelion.tistory.com/4)
+ *   [blog]     "SOSP 2023論文解説: vLLM — PagedAttentionによるKVキャッシュメモリ管理の革新"
+ *   [cb]       "연속 배치 처리 아키텍처" (continuous-batching architecture page)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - KV pools: two arrays, K and V, each [num_blocks][num_heads][block_size][head_dim]
+ *    of fp16 or bf16, row-major.  One (block, head) tile is contiguous.
+ *  - Positions are 0-based: token p of a sequence sits in logical block p / B,
+ *    slot p % B; the block table maps logical block i to a physical block
+ *    ([summary] section 4: 1-based token j in block floor((j-1)/B), slot
+ *    (j-1) mod B).  A "slot" index is physical_block * B + slot.
+ *  - Block tables: int32 [rows][max_blocks_per_seq], row-major, device memory.
+ *    Only the entries that cover a sequence's tokens are read.
+ *  - dtype codes: PA_F16, PA_BF16 for q/K/V; outputs may also be PA_F32.
+ *  - head_dim must be 64 or 128; block_size a multiple of 16 (16..65536).
+ *  - Device pointers are plain CUDA device addresses owned by the caller;
+ *    the library allocates no device memory and keeps no device state.
+ *    `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *    Every launch is asynchronous on that stream.
+ *  - Return value: PA_OK, or an error code for bad arguments detected on the
+ *    host before anything is launched (nothing is launched then).
+ *  - Device-side problems (a table entry outside the pool, a slot outside the
+ *    pool, a context longer than its table, a wait that ran out of time) never
+ *    trap: the kernel ORs a PA_FLAG_* bit into the caller's int32 `err_flag`
+ *    (device memory, zero-initialised by the caller) and skips the bad work.
+ *    pa_get_error() reads and clears it.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------- */
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG 1    /* null pointer, bad size, misaligned pointer */
+#define PA_ERR_UNSUPPORTED 2    /* dtype, head_dim or block_size not supported */
+#define PA_ERR_NO_FREE_BLOCKS 3 /* allocator: pool exhausted ([blog] MemoryError) */
+#define PA_ERR_REFCOUNT 4       /* allocator: reference count would go below 0 */
+#define PA_ERR_BAD_INDEX 5      /* device flag: block / slot / length out of range */
+#define PA_ERR_CUDA 6           /* a CUDA runtime call failed */
+#define PA_ERR_TIMEOUT 7        /* device flag: a bounded wait ran out of time */
+#define PA_ERR_WORKSPACE 8      /* workspace too small */
+
+/* ---- dtypes ------------------------------------------------------------------------ */
+#define PA_F16 0
+#define PA_BF16 1
+#define PA_F32 2
+
+/* ---- device error-flag bits ---------------------------------------------------------- */
+#define PA_FLAG_BAD_BLOCK 1   /* block-table entry or copy pair outside [0, num_blocks) */
+#define PA_FLAG_BAD_SLOT 2    /* slot_mapping entry >= num_blocks * block_size */
+#define PA_FLAG_BAD_LENGTH 4  /* context length < 0, > max_context_len, or > table capacity */
+#define PA_FLAG_TIMEOUT 8     /* an mbarrier wait exceeded its time limit */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int pa_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* pa_status_string(int status);
+
+/* Number of multiprocessors of the current device (0 if no device). */
+int pa_device_sm_count(void);
+
+/*
+ * pa_reshape_and_cache -- slot-scatter write of new K/V into the paged pools.
+ * [blog] "アルゴリズムの擬似コード": append_token stores the token's k and v in
+ * slot num_filled of the sequence's last block.  Here the caller gives each
+ * token's slot directly:
+ *   for t in [0, num_tokens), slot = slot_mapping[t]:
+ *     slot < 0  -> token skipped (padding);
+ *     otherwise K_pool[slot / B][h][slot % B][:] = k_new[t][h][:] for every head h,
+ *               and the same for V (bit copy).
+ * k_new, v_new: device [num_tokens][num_heads][head_dim], dtype `dtype`.
+ * slot_mapping: device int64 [num_tokens].  Slots must be distinct (else the
+ * result for the repeated slot is one of the writers).  A slot >= num_blocks*B
+ * sets PA_FLAG_BAD_SLOT and that token is skipped.  num_tokens == 0 is a no-op.
+ */
+int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                         const int64_t* slot_mapping, int num_tokens, int num_heads, int head_dim,
+                         int block_size, int num_blocks, int dtype, int32_t* err_flag, void* stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write block copy.
+ * [blog] "アルゴリズムの擬似コード" copy_on_write: the new block receives a copy of the
+ * whole source block's K and V ([summary] section 6, parallel sampling).
+ *   for i in [0, n_pairs): (src, dst) = (pairs[2i], pairs[2i+1]):
+ *     K_pool[dst][:][:][:] = K_pool[src][:][:][:], same for V (all heads, all slots).
+ * pairs: device int32 [n_pairs][2].  No block may be both a source and a
+ * destination, and destinations must be distinct (pairs are applied
+ * concurrently).  An id outside [0, num_blocks) sets PA_FLAG_BAD_BLOCK and that
+ * pair is skipped.  n_pairs == 0 is a no-op.
+ */
+int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int n_pairs, int num_heads,
+                   int head_dim, int block_size, int num_blocks, int dtype, int32_t* err_flag, void* stream);
+
+/*
+ * Split-KV partition length (tokens) that pa_decode uses when called with
+ * partition_size == 0: a multiple of 16 between 64 and 1024, chosen from the
+ * batch shape alone (no device query).
+ */
+int pa_decode_partition_size(int num_seqs, int num_heads, int max_context_len);
+
+/*
+ * Bytes of device workspace pa_decode needs for these sizes (partition_size 0 =
+ * the automatic choice above).  0 on bad arguments.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                 int partition_size);
+
+/*
+ * pa_decode -- single-query paged decode attention.
+ * [summary] section 4 equation and Figure 6; [blog] "Attention計算の修正":
+ *   for each sequence s and head h, with n = context_lens[s]:
+ *     x_j = scale * q[s][h] . K_s[j],  j in [0, n), K_s[j] = K_pool[table[s][j/B]][h][j%B]
+ *     out[s][h] = sum_j softmax(x)_j V_s[j]
+ * computed block by block with an online softmax inside each split-KV
+ * partition of `partition_size` tokens and a log-sum-exp combine of the
+ * partitions.  n == 0 gives a zero row.
+ * q: device [num_seqs][num_heads][head_dim], dtype `dtype`.
+ * out: device [num_seqs][num_heads][head_dim], dtype `out_dtype`.
+ * context_lens: device int32 [num_seqs], each <= max_context_len and
+ *   <= max_blocks_per_seq * block_size (else PA_FLAG_BAD_LENGTH, zero row).
+ * workspace: device memory of at least pa_decode_workspace_bytes(...) bytes,
+ *   16-byte aligned; no initial contents required; not to be shared by two
+ *   pa_decode calls that may run at the same time.
+ * partition_size: 0 = automatic, else a multiple of 16 in [16, 1024].
+ * A table entry outside [0, num_blocks) sets PA_FLAG_BAD_BLOCK; the 16-token
+ * chunk it covers is left out of that sequence's sum.
+ * Launches: a one-CTA planning kernel, then the persistent decode kernel
+ * (programmatic dependent launch) on `stream`.
+ */
+int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int max_context_len, int num_seqs, int num_heads, int head_dim, int block_size,
+              int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
+              int partition_size, int32_t* err_flag, void* stream);
+
+/*
+ * pa_prefill_chunk -- causal attention of prefill chunks over paged K/V.
+ * [cb] "Chunked prefill": a long prompt is split into chunks processed over
+ * several steps; [summary] section 4 equation, causal j <= i.
+ *   chunk c holds query rows cu_q_lens[c] .. cu_q_lens[c+1]-1 of q; its row i
+ *   sits at position ctx_before[c] + i of sequence c (block_tables row c) and
+ *   attends positions 0 .. ctx_before[c] + i.  The chunk's own K/V must already
+ *   be in the pools (pa_reshape_and_cache).
+ * q, out: device [total_q][num_heads][head_dim]; q in `dtype`, out in `out_dtype`.
+ * cu_q_lens: device int32 [num_chunks + 1], cu_q_lens[0] == 0, non-decreasing.
+ * ctx_before: device int32 [num_chunks].
+ * total_q: number of rows of q and out (== cu_q_lens[num_chunks]).
+ * max_q_len: host upper bound of any chunk's length (sizes the grid).
+ * Requires head_dim 128, and block_size a multiple of 16 that divides 128 or
+ * is a multiple of 128.  Runs on the tensor cores (tcgen05.mma, accumulators
+ * in tensor memory, tiles moved by TMA).  A chunk whose context runs past
+ * its table sets PA_FLAG_BAD_LENGTH and is skipped; a table entry outside the
+ * pool sets PA_FLAG_BAD_BLOCK and its tokens are left out.
+ */
+int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens,
+                     const int32_t* ctx_before, const void* k_pool, const void* v_pool,
+                     const int32_t* block_tables, int max_blocks_per_seq, int num_chunks, int total_q,
+                     int max_q_len, int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                     int dtype, int32_t* err_flag, void* stream);
+
+/*
+ * pa_get_error -- synchronise `stream`, read the device error flag, clear it.
+ * Returns PA_OK, PA_ERR_TIMEOUT (if PA_FLAG_TIMEOUT is set), PA_ERR_BAD_INDEX
+ * (any other flag) or PA_ERR_CUDA.  If flags_out is non-null it receives the
+ * raw flag bits.
+ */
+int pa_get_error(int32_t* err_flag, int32_t* flags_out, void* stream);
+
+/*
+ * pa_slot_mapping -- host-side slot computation for tokens of sequences whose
+ * block tables the caller already holds (the allocator below does this itself
+ * for the tokens it appends).  [summary] section 4 block mapping:
+ *   slots_out[i] = table[seq_idx[i]][pos[i] / B] * B + pos[i] % B
+ * All arrays are host memory; table is [num_rows][max_blocks_per_seq].
+ * A position whose table entry is negative or beyond max_blocks_per_seq gives
+ * PA_ERR_BAD_INDEX (slots before it are written).
+ */
+int pa_slot_mapping(const int32_t* table, int num_rows, int max_blocks_per_seq, int block_size,
+                    const int32_t* seq_idx, const int32_t* pos, int n, int64_t* slots_out);
+
+/* ---- host block allocator (no CUDA; never on the GPU path) ---------------------
+ * The block manager of [blog] "アルゴリズムの擬似コード" and [summary] sections 5-6:
+ *  - free list initialised to 0..N-1; a block is taken from its END (the first
+ *    block handed out is N-1); taking from an empty list -> PA_ERR_NO_FREE_BLOCKS;
+ *  - a taken block has reference count 1; releasing decrements; at 0 the block
+ *    is appended to the free list;
+ *  - append one token: no block yet -> take one; last block full -> take a new
+ *    one; else last block shared (count > 1) -> copy-on-write: take a new block,
+ *    record (old, new) as a copy pair, drop one reference of the old block and
+ *    put the new block in its place.  The token's slot is (last block)*B + len%B.
+ *  - fork: the child gets the parent's blocks and length; each block +1 reference;
+ *  - free: releases the sequence's blocks in logical order.
+ * A handle is not thread-safe; use one per thread or lock around it.
+ */
+typedef struct pa_alloc pa_alloc;
+
+int pa_alloc_create(int num_blocks, int block_size, pa_alloc** out);
+void pa_alloc_destroy(pa_alloc* a);
+/* New empty sequence.  PA_ERR_INVALID_ARG if seq_id exists or is negative. */
+int pa_alloc_add_seq(pa_alloc* a, int seq_id);
+/* child shares all of parent's blocks.  PA_ERR_INVALID_ARG if parent missing / child exists. */
+int pa_alloc_fork(pa_alloc* a, int parent, int child);
+/*
+ * One new token for each of the n distinct listed sequences, in list order.
+ * slots_out: int64 [n].  copy_pairs_out: int32 [2*n] capacity; receives the
+ * (src, dst) copy-on-write pairs in order, their count in *n_pairs_out.
+ * All-or-nothing: PA_ERR_NO_FREE_BLOCKS leaves the allocator unchanged.
+ */
+int pa_alloc_append_slots(pa_alloc* a, const int* seq_ids, int n, int64_t* slots_out,
+                          int32_t* copy_pairs_out, int* n_pairs_out);
+int pa_alloc_free_seq(pa_alloc* a, int seq_id);
+/* Copy seq's block ids into out[0..cap); *n_blocks and *seq_len receive the sizes
+ * (PA_ERR_INVALID_ARG if cap is too small; sizes are still reported). */
+int pa_alloc_block_table(const pa_alloc* a, int seq_id, int32_t* out, int cap, int* n_blocks, int* seq_len);
+/* Fill rows of a padded table: row i = seq_ids[i]'s blocks, padded with -1 up to
+ * max_blocks_per_seq; ctx_lens_out[i] = its length (either output may be NULL). */
+int pa_alloc_block_tables(const pa_alloc* a, const int* seq_ids, int n, int max_blocks_per_seq,
+                          int32_t* tables_out, int32_t* ctx_lens_out);
+int pa_alloc_num_free(const pa_alloc* a);
+/* Reference count of block_id (-1 if out of range). */
+int pa_alloc_ref(const pa_alloc* a, int block_id);
+/* Number of live sequences. */
+int pa_alloc_num_seqs(const pa_alloc* a);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

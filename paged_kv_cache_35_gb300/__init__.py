@@ -1,0 +1,315 @@
+"""Python binding of libpa (paged KV-cache attention for GB300, sm_103a).
+
+Argument marshalling only: every function here checks shapes and dtypes,
+takes raw device pointers from torch tensors and the current CUDA stream,
+and calls the C ABI declared in ``include/pa.h``.  All computation runs in
+the library's CUDA kernels (or, for the block allocator, its host C++).
+There is no fallback: if ``libpa.so`` has not been built, every call raises.
+
+Names match the C entry points: ``pa_reshape_and_cache``, ``pa_copy_blocks``,
+``pa_decode``, ``pa_prefill_chunk``, ``pa_get_error``, ``pa_slot_mapping``,
+and the ``pa_alloc_*`` allocator (wrapped by :class:`BlockAllocator`).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpa.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_NO_FREE_BLOCKS = 3
+PA_ERR_REFCOUNT = 4
+PA_ERR_BAD_INDEX = 5
+PA_ERR_CUDA = 6
+PA_ERR_TIMEOUT = 7
+PA_ERR_WORKSPACE = 8
+
+PA_F16, PA_BF16, PA_F32 = 0, 1, 2
+
+PA_FLAG_BAD_BLOCK = 1
+PA_FLAG_BAD_SLOT = 2
+PA_FLAG_BAD_LENGTH = 4
+PA_FLAG_TIMEOUT = 8
+
+_TORCH_TO_PA = {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.float32: PA_F32}
+
+# Every function the header declares, with its ctypes signature.
+_P, _I, _L, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "pa_version": ([], _I),
+    "pa_status_string": ([_I], ctypes.c_char_p),
+    "pa_device_sm_count": ([], _I),
+    "pa_reshape_and_cache": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pa_copy_blocks": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pa_decode_partition_size": ([_I, _I, _I], _I),
+    "pa_decode_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
+    "pa_decode": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _I, _P, _P], _I),
+    "pa_prefill_chunk": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P], _I),
+    "pa_get_error": ([_P, _P, _P], _I),
+    "pa_slot_mapping": ([_P, _I, _I, _I, _P, _P, _I, _P], _I),
+    "pa_alloc_create": ([_I, _I, _P], _I),
+    "pa_alloc_destroy": ([_P], None),
+    "pa_alloc_add_seq": ([_P, _I], _I),
+    "pa_alloc_fork": ([_P, _I, _I], _I),
+    "pa_alloc_append_slots": ([_P, _P, _I, _P, _P, _P], _I),
+    "pa_alloc_free_seq": ([_P, _I], _I),
+    "pa_alloc_block_table": ([_P, _I, _P, _I, _P, _P], _I),
+    "pa_alloc_block_tables": ([_P, _P, _I, _I, _P, _P], _I),
+    "pa_alloc_num_free": ([_P], _I),
+    "pa_alloc_ref": ([_P, _I], _I),
+    "pa_alloc_num_seqs": ([_P], _I),
+}
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C-ABI library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        raise PAError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, has {t.dim()}")
+    return t.data_ptr()
+
+
+def _kv_code(t: torch.Tensor) -> int:
+    if t.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError(f"K/V/q must be float16 or bfloat16, got {t.dtype}")
+    return _TORCH_TO_PA[t.dtype]
+
+
+def new_error_flag(device=None) -> torch.Tensor:
+    """A zeroed device int32 for the kernels' error bits."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+# ---- GPU entry points ---------------------------------------------------------------
+
+def pa_reshape_and_cache(k_new, v_new, k_pool, v_pool, slot_mapping, err_flag, stream=None):
+    """Scatter k_new/v_new [T][H][D] into pools [NB][H][B][D] at slot_mapping[T] (int64)."""
+    NB, H, B, D = k_pool.shape
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, H, D) or tuple(v_new.shape) != (T, H, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("shape mismatch")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    dt = _kv_code(k_pool)
+    st = lib().pa_reshape_and_cache(
+        _dev(k_new, "k_new", k_pool.dtype), _dev(v_new, "v_new", k_pool.dtype), _dev(k_pool, "k_pool"),
+        _dev(v_pool, "v_pool", k_pool.dtype), _dev(slot_mapping, "slot_mapping", torch.int64), T, H, D, B, NB, dt,
+        _dev(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_pool, v_pool, pairs, err_flag, stream=None):
+    """Copy whole blocks: pairs int32 [n][2] of (src, dst)."""
+    NB, H, B, D = k_pool.shape
+    n = pairs.shape[0] if pairs.numel() else 0
+    if n and tuple(pairs.shape) != (n, 2):
+        raise ValueError("pairs must be [n][2]")
+    st = lib().pa_copy_blocks(
+        _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        _dev(pairs, "pairs", torch.int32) if n else None, n, H, D, B, NB, _kv_code(k_pool),
+        _dev(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+def pa_decode_partition_size(num_seqs: int, num_heads: int, max_context_len: int) -> int:
+    return int(lib().pa_decode_partition_size(num_seqs, num_heads, max_context_len))
+
+
+def pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size=0) -> int:
+    return int(lib().pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size))
+
+
+def decode_workspace(num_seqs, num_heads, head_dim, max_context_len, partition_size=0, device=None):
+    """A uint8 device tensor big enough for pa_decode with these sizes."""
+    n = pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size)
+    if n == 0:
+        raise ValueError("bad sizes for the decode workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, max_context_len, scale, workspace, err_flag,
+              partition_size=0, stream=None):
+    """out[S][H][D] = paged decode attention of q[S][H][D]."""
+    NB, H, B, D = k_pool.shape
+    S = q.shape[0]
+    if tuple(q.shape) != (S, H, D) or tuple(out.shape) != (S, H, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] < S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [>=S][MB], context_lens [S]")
+    st = lib().pa_decode(
+        _dev(out, "out", (torch.float16, torch.bfloat16, torch.float32)), _TORCH_TO_PA[out.dtype],
+        _dev(q, "q", k_pool.dtype), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, D, B, NB, float(scale),
+        _kv_code(k_pool), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        int(partition_size), _dev(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "pa_decode")
+
+
+def pa_prefill_chunk(out, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables, max_q_len, scale, err_flag,
+                     stream=None):
+    """Causal attention of prefill chunks: q, out [total][H][D]."""
+    NB, H, B, D = k_pool.shape
+    T = q.shape[0]
+    C = ctx_before.shape[0]
+    if tuple(q.shape) != (T, H, D) or tuple(out.shape) != (T, H, D) or cu_q_lens.shape != (C + 1,):
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] < C:
+        raise ValueError("block_tables must be [>=C][MB]")
+    st = lib().pa_prefill_chunk(
+        _dev(out, "out", (torch.float16, torch.bfloat16, torch.float32)), _TORCH_TO_PA[out.dtype],
+        _dev(q, "q", k_pool.dtype), _dev(cu_q_lens, "cu_q_lens", torch.int32),
+        _dev(ctx_before, "ctx_before", torch.int32), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1], C, T, int(max_q_len), H, D, B, NB,
+        float(scale), _kv_code(k_pool), _dev(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "pa_prefill_chunk")
+
+
+def pa_get_error(err_flag, stream=None) -> int:
+    """Synchronise, read and clear the device error flag; returns its bits."""
+    bits = ctypes.c_int32(0)
+    st = lib().pa_get_error(_dev(err_flag, "err_flag", torch.int32), ctypes.addressof(bits), _stream(stream))
+    if st not in (PA_OK, PA_ERR_BAD_INDEX, PA_ERR_TIMEOUT):
+        raise PAError(st, "pa_get_error")
+    return int(bits.value)
+
+
+# ---- host entry points --------------------------------------------------------------
+
+def _host_i32(a) -> np.ndarray:
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def pa_slot_mapping(block_tables, seq_idx, pos, block_size: int) -> np.ndarray:
+    """Host slots of (sequence row, position) pairs through host block tables."""
+    tb = _host_i32(block_tables)
+    si = _host_i32(seq_idx)
+    ps = _host_i32(pos)
+    out = np.zeros(si.shape[0], dtype=np.int64)
+    st = lib().pa_slot_mapping(tb.ctypes.data, tb.shape[0], tb.shape[1], block_size, si.ctypes.data, ps.ctypes.data,
+                               si.shape[0], out.ctypes.data)
+    _check(st, "pa_slot_mapping")
+    return out
+
+
+class BlockAllocator:
+    """Host block manager (free list, reference counts, copy-on-write)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self.block_size = block_size
+        self.num_blocks = num_blocks
+        h = ctypes.c_void_p()
+        _check(lib().pa_alloc_create(num_blocks, block_size, ctypes.byref(h)), "pa_alloc_create")
+        self._h = h
+
+    def close(self):
+        if self._h:
+            lib().pa_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_seq(self, seq_id: int):
+        _check(lib().pa_alloc_add_seq(self._h, seq_id), "pa_alloc_add_seq")
+
+    def fork(self, parent: int, child: int):
+        _check(lib().pa_alloc_fork(self._h, parent, child), "pa_alloc_fork")
+
+    def append_slots(self, seq_ids):
+        """One token per listed sequence -> (slots int64 [n], pairs int32 [k][2])."""
+        ids = _host_i32(list(seq_ids))
+        n = ids.shape[0]
+        slots = np.zeros(n, dtype=np.int64)
+        pairs = np.zeros((max(n, 1), 2), dtype=np.int32)
+        npairs = ctypes.c_int(0)
+        _check(lib().pa_alloc_append_slots(self._h, ids.ctypes.data, n, slots.ctypes.data, pairs.ctypes.data,
+                                           ctypes.byref(npairs)), "pa_alloc_append_slots")
+        return slots, pairs[: npairs.value].copy()
+
+    def free_seq(self, seq_id: int):
+        _check(lib().pa_alloc_free_seq(self._h, seq_id), "pa_alloc_free_seq")
+
+    def block_table(self, seq_id: int):
+        nb, ln = ctypes.c_int(0), ctypes.c_int(0)
+        lib().pa_alloc_block_table(self._h, seq_id, None, 0, ctypes.byref(nb), ctypes.byref(ln))
+        out = np.zeros(max(nb.value, 1), dtype=np.int32)
+        _check(lib().pa_alloc_block_table(self._h, seq_id, out.ctypes.data, out.shape[0], ctypes.byref(nb),
+                                          ctypes.byref(ln)), "pa_alloc_block_table")
+        return out[: nb.value].tolist(), ln.value
+
+    def block_tables(self, seq_ids, max_blocks_per_seq: int):
+        """(tables int32 [n][max_blocks_per_seq] padded with -1, lengths int32 [n])."""
+        ids = _host_i32(list(seq_ids))
+        n = ids.shape[0]
+        tables = np.zeros((n, max_blocks_per_seq), dtype=np.int32)
+        lens = np.zeros(n, dtype=np.int32)
+        _check(lib().pa_alloc_block_tables(self._h, ids.ctypes.data, n, max_blocks_per_seq, tables.ctypes.data,
+                                           lens.ctypes.data), "pa_alloc_block_tables")
+        return tables, lens
+
+    def num_free(self) -> int:
+        return int(lib().pa_alloc_num_free(self._h))
+
+    def ref(self, block_id: int) -> int:
+        return int(lib().pa_alloc_ref(self._h, block_id))
+
+    def num_seqs(self) -> int:
+        return int(lib().pa_alloc_num_seqs(self._h))

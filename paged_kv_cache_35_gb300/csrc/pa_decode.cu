@@ -1,0 +1,641 @@
+// Paged decode attention for sm_103a.
+//
+// Method: PagedAttention ("Efficient Memory Management for Large Language
+// Model Serving with PagedAttention"), paper-summary page section 4 and
+// Figure 6: one query per sequence attends to K/V kept in fixed-size,
+// non-contiguous blocks found through a per-sequence block table.  The blog
+// page ("SOSP 2023論文解説: vLLM", section "Attention計算の修正") states the
+// result as softmax(q [K_1 | ... | K_n]^T / sqrt(d)) [V_1 | ... | V_n],
+// computed block by block with an online softmax.
+//
+// Design (ours, for one GB300):
+//  * The context of every sequence is cut into split-KV partitions of P
+//    tokens; a unit of work is one (sequence, head, partition).  A one-CTA
+//    planning kernel lists the (sequence, partition) items longest first
+//    (counting sort on the partition's 16-token chunk count) so the
+//    persistent grid finishes with short units.
+//  * The decode kernel is persistent (SM count x resident CTAs) and warp
+//    specialised:
+//      warp 5  (scheduler) takes unit ids from a global counter, reads the
+//              item, the context length and the table entries of the unit
+//              into a 4-deep unit queue in shared memory, and bulk-copies
+//              the unit's query row next to them;
+//      warp 4  (producer)  streams the unit's 16-token K and V tiles (one
+//              contiguous 16*D*2-byte run each in the [NB][H][B][D] pools)
+//              into an 8-stage shared-memory ring with cp.async.bulk,
+//              completion counted in bytes on one mbarrier per stage;
+//      warps 0-3 (consumers) take every 4th tile of the unit: 8 lanes per
+//              token row, 16-byte shared loads (conflict free), fp32 dot
+//              products reduced with 3 shuffles, online softmax (running max
+//              and sum, base-2 exponent with log2(e) folded into the query).
+//    The four consumer warps merge their (max, sum, output) through shared
+//    memory; a unit that is the only partition of its sequence writes the
+//    output directly.  Otherwise it writes its normalised partial and
+//    (max, sum) to the workspace, and the warp that completes the last
+//    partition of a (sequence, head) merges all partitions with the
+//    log-sum-exp rule in partition order (so the result does not depend on
+//    scheduling, nor on which physical blocks hold the tokens).
+//  * Every wait is bounded; bad table entries are flagged, never trapped.
+#include <math.h>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+constexpr int kChunk = 16;                    // tokens per ring stage
+constexpr int kConsumerWarps = 4;
+constexpr int kProducerWarp = kConsumerWarps;  // warp 4
+constexpr int kSchedulerWarp = kConsumerWarps + 1;
+constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;
+constexpr int kStages = 8;
+constexpr int kUnitQueue = 4;
+constexpr int kMaxPartition = 1024;
+constexpr int kMaxChunksPerUnit = kMaxPartition / kChunk;
+constexpr int kPlanThreads = 1024;
+
+struct DecodeArgs {
+  void* out;
+  int out_dtype;
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int max_context_len;
+  int num_seqs;
+  int num_heads;
+  int block_size;
+  int num_blocks;
+  float qscale;  // scale * log2(e)
+  int partition_size;
+  int max_parts;
+  int* counters;   // [0] unit counter, [1] item count, [2 + s*H + h] partition arrivals
+  int2* items;     // (sequence, partition) in processing order
+  float2* part_ml; // [S][H][max_parts] (max, sum) in log2 units
+  float* part_o;   // [S][H][max_parts][D] normalised partial outputs
+  int32_t* err_flag;
+};
+
+template <int D, typename T>
+struct DecodeSmem {
+  T ring[kStages][2][kChunk * D];  // K tile, V tile
+  T qbuf[kUnitQueue][D];
+  int32_t chunk_blk[kUnitQueue][kMaxChunksPerUnit];
+  int4 unit[kUnitQueue];  // sequence, head, partition, tokens in partition
+  int unit_nparts[kUnitQueue];
+  float co[2][kConsumerWarps][D];
+  float cm[2][kConsumerWarps];
+  float cl[2][kConsumerWarps];
+  int slot_ok[kStages];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t ufull[kUnitQueue];
+  uint64_t uempty[kUnitQueue];
+  uint64_t comb[2];
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool length_ok(const DecodeArgs& a, int ctx) {
+  return ctx >= 0 && ctx <= a.max_context_len && (int64_t)ctx <= (int64_t)a.max_blocks_per_seq * a.block_size;
+}
+
+// ---------------------------------------------------------------------------------
+// Planning kernel: one CTA.  Lists the (sequence, partition) items, longest
+// first; resets the unit counter and the per-(sequence, head) arrival
+// counters; writes zero rows for empty or invalid sequences.
+template <int D>
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) {
+  griddep_launch_dependents();
+  extern __shared__ int plan_smem[];
+  const int P = a.partition_size;
+  const int nb = P / kChunk;  // buckets: chunks in an item, 1..nb
+  int* hist = plan_smem;
+  int* offs = plan_smem + nb;
+  int* cur = plan_smem + 2 * nb;
+  const int tid = threadIdx.x;
+  const int S = a.num_seqs, H = a.num_heads;
+  for (int i = tid; i < nb; i += blockDim.x) {
+    hist[i] = 0;
+    cur[i] = 0;
+  }
+  for (int i = tid; i < S * H; i += blockDim.x) a.counters[2 + i] = 0;
+  __syncthreads();
+  for (int s = tid; s < S; s += blockDim.x) {
+    const int ctx = __ldg(a.context_lens + s);
+    if (!length_ok(a, ctx) || ctx == 0) continue;
+    const int np = (ctx + P - 1) / P;
+    const int last = ctx - (np - 1) * P;
+    if (np > 1) atomicAdd(&hist[nb - 1], np - 1);
+    atomicAdd(&hist[(last + kChunk - 1) / kChunk - 1], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int b = nb - 1; b >= 0; --b) {
+      offs[b] = acc;
+      acc += hist[b];
+    }
+    a.counters[0] = 0;
+    a.counters[1] = acc;
+  }
+  __syncthreads();
+  for (int s = tid; s < S; s += blockDim.x) {
+    const int ctx = __ldg(a.context_lens + s);
+    if (!length_ok(a, ctx) || ctx == 0) {
+      if (ctx != 0) atomicOr(a.err_flag, PA_FLAG_BAD_LENGTH);
+      for (int i = 0; i < H * D; ++i) store_out(a.out, (size_t)s * H * D + i, a.out_dtype, 0.f);
+      continue;
+    }
+    const int np = (ctx + P - 1) / P;
+    const int last = ctx - (np - 1) * P;
+    if (np > 1) {
+      const int base = offs[nb - 1] + atomicAdd(&cur[nb - 1], np - 1);
+      for (int p = 0; p < np - 1; ++p) a.items[base + p] = make_int2(s, p);
+    }
+    const int lb = (last + kChunk - 1) / kChunk - 1;
+    a.items[offs[lb] + atomicAdd(&cur[lb], 1)] = make_int2(s, np - 1);
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Consumer: one 16-token tile.  Lane (t4 = lane/8, c = lane%8) owns tokens
+// t4, t4+4, t4+8, t4+12 of the tile and the 16-byte vectors c (+8) of each
+// row: a group of 8 lanes reads one 128-byte stretch of a row, so the
+// shared-memory loads are conflict free.
+template <int D, typename T>
+__device__ __forceinline__ void consume_tile(const T* __restrict__ Ks, const T* __restrict__ Vs, int nvalid,
+                                             const float* qf, float& m, float& l, float* o, int lane) {
+  constexpr int VPL = D / 64;
+  const int t4 = lane >> 3;
+  const int c = lane & 7;
+  float sc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int tok = t4 + 4 * i;
+    const T* row = Ks + tok * D;
+    float acc = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const uint4 u = *reinterpret_cast<const uint4*>(row + (c + 8 * v) * 8);
+      float f[8];
+      Elt<T>::to_float8(u, f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(qf[v * 8 + e], f[e], acc);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    sc[i] = tok < nvalid ? acc : -INFINITY;
+  }
+  float cmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+  cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 8));
+  cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 16));
+  const float m_new = fmaxf(m, cmax);
+  const float alpha = exp2f(m - m_new);
+  float pr[4];
+  float psum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    pr[i] = exp2f(sc[i] - m_new);
+    psum += pr[i];
+  }
+  l = l * alpha + psum;
+#pragma unroll
+  for (int e = 0; e < 8 * VPL; ++e) o[e] *= alpha;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int tok = t4 + 4 * i;
+    if (tok < nvalid) {  // rows past the context may hold any bits (even NaN)
+      const T* row = Vs + tok * D;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const uint4 u = *reinterpret_cast<const uint4*>(row + (c + 8 * v) * 8);
+        float f[8];
+        Elt<T>::to_float8(u, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[v * 8 + e] = fmaf(pr[i], f[e], o[v * 8 + e]);
+      }
+    }
+  }
+  m = m_new;
+}
+
+// Merge of all partitions of one (sequence, head) by one warp, in partition
+// order: M = max m_p, out = sum_p 2^(m_p - M) l_p o_p / sum_p 2^(m_p - M) l_p.
+template <int D>
+__device__ __forceinline__ void merge_partitions(const DecodeArgs& a, int s, int h, int nparts, int lane) {
+  const size_t base = ((size_t)s * a.num_heads + h) * a.max_parts;
+  float M = -INFINITY;
+  for (int p = 0; p < nparts; ++p) M = fmaxf(M, __ldcg(&a.part_ml[base + p].x));
+  float L = 0.f;
+  float O[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) O[i] = 0.f;
+  for (int p = 0; p < nparts; ++p) {
+    const float mp = __ldcg(&a.part_ml[base + p].x);
+    const float lp = __ldcg(&a.part_ml[base + p].y);
+    const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - M) * lp;
+    L += w;
+    const float* op = a.part_o + (base + p) * D;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) O[i] = fmaf(w, __ldcg(op + lane + 32 * i), O[i]);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const size_t ob = ((size_t)s * a.num_heads + h) * D;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) store_out(a.out, ob + lane + 32 * i, a.out_dtype, O[i] * inv);
+  if (lane == 0) a.counters[2 + s * a.num_heads + h] = 0;
+}
+
+template <int D, typename T>
+__device__ __forceinline__ void run_scheduler(const DecodeArgs& a, DecodeSmem<D, T>& sm, int lane) {
+  volatile int* abort_flag = &sm.abort_flag;
+  const int H = a.num_heads;
+  const int P = a.partition_size;
+  const long long total_units = (long long)__ldg(a.counters + 1) * H;
+  int issued = 0;
+  for (int k = 0;; ++k) {
+    const int qs = k % kUnitQueue;
+    const uint32_t par = (k / kUnitQueue) & 1;
+    int u = 0;
+    if (lane == 0) u = atomicAdd(a.counters, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(&sm.uempty[qs], par ^ 1, abort_flag, a.err_flag);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    if ((long long)u >= total_units) {
+      if (lane == 0) {
+        sm.unit[qs] = make_int4(-1, 0, 0, 0);
+        mbar_arrive(&sm.ufull[qs]);
+      }
+      break;
+    }
+    const int item = u / H;
+    const int h = u - item * H;
+    const int2 it = __ldg(a.items + item);
+    const int s = it.x;
+    const int p = it.y;
+    const int ctx = __ldg(a.context_lens + s);
+    const int tok0 = p * P;
+    const int ntok = min(P, ctx - tok0);
+    const int nchunks = (ntok + kChunk - 1) / kChunk;
+    const int32_t* trow = a.block_tables + (size_t)s * a.max_blocks_per_seq;
+    for (int j = lane; j < nchunks; j += 32) sm.chunk_blk[qs][j] = __ldg(trow + (tok0 + j * kChunk) / a.block_size);
+    __syncwarp();
+    if (lane == 0) {
+      sm.unit[qs] = make_int4(s, h, p, ntok);
+      sm.unit_nparts[qs] = (ctx + P - 1) / P;
+      __threadfence_block();
+      mbar_arrive_expect_tx(&sm.ufull[qs], D * sizeof(T));
+      bulk_g2s(sm.qbuf[qs], static_cast<const T*>(a.q) + ((size_t)s * H + h) * D, D * sizeof(T), &sm.ufull[qs]);
+    }
+    ++issued;
+  }
+  if (lane == 0 && *abort_flag) {  // let in-flight query copies land before exit
+    for (int kk = max(0, issued - kUnitQueue); kk < issued; ++kk)
+      mbar_wait_drain(&sm.ufull[kk % kUnitQueue], (kk / kUnitQueue) & 1);
+  }
+}
+
+template <int D, typename T>
+__device__ __forceinline__ void run_producer(const DecodeArgs& a, DecodeSmem<D, T>& sm) {
+  constexpr uint32_t kTileBytes = kChunk * D * sizeof(T);
+  volatile int* abort_flag = &sm.abort_flag;
+  const int H = a.num_heads;
+  const int B = a.block_size;
+  const int P = a.partition_size;
+  const T* kp = static_cast<const T*>(a.k_pool);
+  const T* vp = static_cast<const T*>(a.v_pool);
+  uint32_t g = 0;
+  bool aborted = false;
+  for (int k = 0; !aborted; ++k) {
+    const int qs = k % kUnitQueue;
+    if (!mbar_wait(&sm.ufull[qs], (k / kUnitQueue) & 1, abort_flag, a.err_flag)) break;
+    const int4 un = sm.unit[qs];
+    if (un.x < 0) break;
+    const int h = un.y;
+    const int tok0 = un.z * P;
+    const int nchunks = (un.w + kChunk - 1) / kChunk;
+    for (int j = 0; j < nchunks; ++j) {
+      const int slot = g % kStages;
+      if (!mbar_wait(&sm.empty[slot], ((g / kStages) & 1) ^ 1, abort_flag, a.err_flag)) {
+        aborted = true;
+        break;
+      }
+      const int32_t blk = sm.chunk_blk[qs][j];
+      if (blk >= 0 && blk < a.num_blocks) {
+        const int off = (tok0 + j * kChunk) % B;
+        const size_t base = (((size_t)blk * H + h) * B + off) * D;
+        sm.slot_ok[slot] = 1;
+        mbar_arrive_expect_tx(&sm.full[slot], 2 * kTileBytes);
+        bulk_g2s(sm.ring[slot][0], kp + base, kTileBytes, &sm.full[slot]);
+        bulk_g2s(sm.ring[slot][1], vp + base, kTileBytes, &sm.full[slot]);
+      } else {
+        sm.slot_ok[slot] = 0;
+        atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
+        mbar_arrive(&sm.full[slot]);
+      }
+      ++g;
+    }
+    if (!aborted) mbar_arrive(&sm.uempty[qs]);
+  }
+  if (*abort_flag) {  // let in-flight tile copies land before exit
+    const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0;
+    for (uint32_t gg = first; gg < g; ++gg) mbar_wait_drain(&sm.full[gg % kStages], (gg / kStages) & 1);
+  }
+}
+
+template <int D, typename T>
+__device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, T>& sm, int warp, int lane) {
+  constexpr int VPL = D / 64;
+  volatile int* abort_flag = &sm.abort_flag;
+  const int H = a.num_heads;
+  const int c = lane & 7;
+  uint32_t g = 0;
+  for (int k = 0;; ++k) {
+    const int qs = k % kUnitQueue;
+    bool ok = mbar_wait(&sm.ufull[qs], (k / kUnitQueue) & 1, abort_flag, a.err_flag);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const int4 un = sm.unit[qs];
+    if (un.x < 0) break;
+    const int nparts = sm.unit_nparts[qs];
+    float qf[8 * VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const uint4 u = *reinterpret_cast<const uint4*>(&sm.qbuf[qs][(c + 8 * v) * 8]);
+      Elt<T>::to_float8(u, qf + 8 * v);
+    }
+#pragma unroll
+    for (int e = 0; e < 8 * VPL; ++e) qf[e] *= a.qscale;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.uempty[qs]);
+
+    const int ntok = un.w;
+    const int nchunks = (ntok + kChunk - 1) / kChunk;
+    float m = -INFINITY, l = 0.f;
+    float o[8 * VPL];
+#pragma unroll
+    for (int e = 0; e < 8 * VPL; ++e) o[e] = 0.f;
+    bool aborted = false;
+    for (int j = warp; j < nchunks; j += kConsumerWarps) {
+      const uint32_t gg = g + j;
+      const int slot = gg % kStages;
+      ok = mbar_wait(&sm.full[slot], (gg / kStages) & 1, abort_flag, a.err_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        aborted = true;
+        break;
+      }
+      if (sm.slot_ok[slot]) {
+        consume_tile<D, T>(sm.ring[slot][0], sm.ring[slot][1], min(kChunk, ntok - j * kChunk), qf, m, l, o, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    }
+    if (aborted) break;
+    g += nchunks;
+
+    // merge the 4 token groups of the warp
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+#pragma unroll
+    for (int e = 0; e < 8 * VPL; ++e) {
+      o[e] += __shfl_xor_sync(0xffffffffu, o[e], 8);
+      o[e] += __shfl_xor_sync(0xffffffffu, o[e], 16);
+    }
+    const int cb = k & 1;
+    if (lane < 8) {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sm.co[cb][warp][(lane + 8 * v) * 8 + e] = o[v * 8 + e];
+    }
+    if (lane == 0) {
+      sm.cm[cb][warp] = m;
+      sm.cl[cb][warp] = l;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.comb[cb]);
+    ok = mbar_wait(&sm.comb[cb], (k >> 1) & 1, abort_flag, a.err_flag);
+    if (!__all_sync(0xffffffffu, ok)) break;
+
+    // merge the consumer warps: thread t owns output dimension t
+    if (warp < D / 32) {
+      const int t = warp * 32 + lane;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.cm[cb][w]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = sm.cm[cb][w];
+        const float wt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        L = fmaf(wt, sm.cl[cb][w], L);
+        O = fmaf(wt, sm.co[cb][w][t], O);
+      }
+      const int s = un.x, h = un.y, p = un.z;
+      const float val = L > 0.f ? O / L : 0.f;
+      if (nparts == 1) {
+        store_out(a.out, ((size_t)s * H + h) * D + t, a.out_dtype, val);
+      } else {
+        const size_t pidx = ((size_t)s * H + h) * a.max_parts + p;
+        a.part_o[pidx * D + t] = val;
+        if (t == 0) a.part_ml[pidx] = make_float2(M, L);
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(&a.counters[2 + s * H + h], 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == nparts * (D / 32) - 1) {
+          __threadfence();
+          merge_partitions<D>(a, s, h, nparts, lane);
+        }
+      }
+    }
+  }
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t decode_smem_raw[];
+  auto& sm = *reinterpret_cast<DecodeSmem<D, T>*>(decode_smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], 1);
+    }
+    for (int i = 0; i < kUnitQueue; ++i) {
+      mbar_init(&sm.ufull[i], 1);
+      mbar_init(&sm.uempty[i], kConsumerWarps + 1);
+    }
+    mbar_init(&sm.comb[0], kConsumerWarps);
+    mbar_init(&sm.comb[1], kConsumerWarps);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  griddep_wait();  // the planning kernel's list and counters are visible from here
+  if (warp == kSchedulerWarp) {
+    run_scheduler<D, T>(a, sm, lane);
+  } else if (warp == kProducerWarp) {
+    if (lane == 0) run_producer<D, T>(a, sm);
+  } else {
+    run_consumer<D, T>(a, sm, warp, lane);
+  }
+}
+
+}  // namespace pa
+
+// ---------------------------------------------------------------------------------
+// Host side
+namespace {
+
+struct WsLayout {
+  size_t counters, items, ml, o, total;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WsLayout ws_layout(int S, int H, int D, int max_parts) {
+  WsLayout w;
+  size_t off = 0;
+  w.counters = off;
+  off = align_up(off + sizeof(int) * (2 + (size_t)S * H), 256);
+  w.items = off;
+  off = align_up(off + sizeof(int2) * (size_t)S * max_parts, 256);
+  w.ml = off;
+  off = align_up(off + sizeof(float2) * (size_t)S * H * max_parts, 256);
+  w.o = off;
+  off = align_up(off + sizeof(float) * (size_t)S * H * max_parts * D, 256);
+  w.total = off;
+  return w;
+}
+
+int resolve_partition(int S, int H, int max_ctx, int partition_size) {
+  if (partition_size == 0) return pa_decode_partition_size(S, H, max_ctx);
+  return partition_size;
+}
+
+template <int D, typename T>
+int launch_decode(const pa::DecodeArgs& a, cudaStream_t stream) {
+  using Smem = pa::DecodeSmem<D, T>;
+  const int smem = (int)sizeof(Smem);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  static int configured[64] = {0};
+  static int occupancy[64] = {0};
+  if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(pa::decode_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pa::decode_kernel<D, T>, pa::kDecodeThreads, smem) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    occupancy[dev] = occ > 0 ? occ : 1;
+    configured[dev] = 1;
+  }
+  const int sms = pa_host::device_sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+
+  const int nb = a.partition_size / pa::kChunk;
+  pa::plan_kernel<D><<<1, pa::kPlanThreads, 3 * nb * sizeof(int), stream>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+
+  const long long max_units = (long long)a.num_seqs * a.num_heads * a.max_parts;
+  long long grid = (long long)sms * occupancy[dev];
+  if (grid > max_units) grid = max_units;
+  if (grid < 1) grid = 1;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(pa::kDecodeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, pa::decode_kernel<D, T>, a) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_partition_size(int num_seqs, int num_heads, int max_context_len) {
+  if (num_seqs <= 0 || num_heads <= 0 || max_context_len <= 0) return 512;
+  int P = 512;
+  while (P > 64 && (long long)num_seqs * num_heads * ((max_context_len + P - 1) / P) < 1216) P /= 2;
+  return P;
+}
+
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                 int partition_size) {
+  if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+  const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
+  if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return 0;
+  const int max_parts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
+  return ws_layout(num_seqs, num_heads, head_dim, max_parts).total;
+}
+
+int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+              int num_seqs, int num_heads, int head_dim, int block_size, int num_blocks, float scale, int dtype,
+              void* workspace, size_t workspace_bytes, int partition_size, int32_t* err_flag, void* stream) {
+  if (!pa_host::is_kv_dtype(dtype) || !pa_host::is_out_dtype(out_dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size <= 0 || block_size % pa::kChunk != 0 || block_size > 65536) return PA_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens || !workspace || !err_flag)
+    return PA_ERR_INVALID_ARG;
+  if (!pa_host::aligned16(q) || !pa_host::aligned16(k_pool) || !pa_host::aligned16(v_pool) ||
+      !pa_host::aligned16(workspace) || !pa_host::aligned16(out))
+    return PA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if ((long long)num_seqs * num_heads > (1ll << 30)) return PA_ERR_INVALID_ARG;
+  const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
+  if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return PA_ERR_INVALID_ARG;
+  const int max_parts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
+  const WsLayout w = ws_layout(num_seqs, num_heads, head_dim, max_parts);
+  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+
+  pa::DecodeArgs a;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.max_context_len = max_context_len;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.qscale = scale * 1.4426950408889634f;
+  a.partition_size = P;
+  a.max_parts = max_parts;
+  char* ws = static_cast<char*>(workspace);
+  a.counters = reinterpret_cast<int*>(ws + w.counters);
+  a.items = reinterpret_cast<int2*>(ws + w.items);
+  a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
+  a.part_o = reinterpret_cast<float*>(ws + w.o);
+  a.err_flag = err_flag;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (head_dim == 128) {
+    return dtype == PA_F16 ? launch_decode<128, __half>(a, s) : launch_decode<128, __nv_bfloat16>(a, s);
+  }
+  return dtype == PA_F16 ? launch_decode<64, __half>(a, s) : launch_decode<64, __nv_bfloat16>(a, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,614 @@
+// Chunked-prefill attention over paged K/V on the sm_103a tensor cores.
+//
+// Method: the continuous-batching page ("연속 배치 처리 아키텍처", section
+// "Chunked prefill") splits a long prompt into chunks that run over several
+// steps; each chunk's queries attend causally (the j <= i of the section 4
+// equation of the PagedAttention paper summary) to the sequence's paged K/V,
+// which already holds every earlier token and the chunk's own tokens.
+//
+// Design (ours, for one GB300):
+//  * One CTA per (128-query tile, head, chunk), 6 warps:
+//      warp 5  (loader)   TMA: the query tile once (3-D tensor map over
+//              [token][head][dim]) and, per 128-key tile, the K and V rows of
+//              the pages that hold those keys (2-D tensor map over the pool
+//              seen as [block*H*B + slot][dim]), into a 2-stage ring;
+//      warp 4  (MMA)      one thread issues tcgen05.mma (kind::f16, M=N=128,
+//              K=16 per instruction, fp32 accumulators in tensor memory):
+//              S_j = Q K_j^T into one of two TMEM score buffers, then
+//              O += P_j V_j into the TMEM output accumulator;
+//      warps 0-3 (softmax) thread i owns query row i = TMEM lane i: it reads
+//              its score row with tcgen05.ld, applies the causal / context
+//              mask, runs the online softmax, and writes its probability row
+//              as bf16/fp16 into a shared-memory operand for the P V product.
+//    S_{j+1} is issued before P_j V_j, so the softmax of tile j+1 overlaps
+//    the tensor-core work of tile j.
+//  * Operands are 128-byte-swizzled: K-major for Q, K and P; V is consumed
+//    MN-major (dims contiguous), straight from the pool layout.
+//  * The output accumulator is rescaled lazily: only when a row's running max
+//    grows by more than 2^8 (then O is read, scaled and written back in
+//    tensor memory); otherwise the stale max is kept, which is exact because
+//    the same max is used for the row sum.
+//  * Keys past the context, keys of pages whose table entry is bad, and keys
+//    past a query's position are masked; V rows that were not loaded or lie
+//    past the context are zeroed in shared memory so that stale or NaN bits
+//    cannot reach the P V product.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+constexpr int kPfRows = 128;   // query rows per CTA (MMA M)
+constexpr int kPfKeys = 128;   // keys per tile (N of S = Q K^T, K of O += P V)
+constexpr int kPfD = 128;      // head_dim
+constexpr int kPfThreads = 192;
+constexpr int kPfMmaWarp = 4;
+constexpr int kPfLoadWarp = 5;
+constexpr uint32_t kHalfBytes = kPfRows * 64 * 2;  // 128 rows x 64 columns x 2 bytes
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;     // one 128 x 128 16-bit tile
+constexpr float kRescaleThreshold = 8.0f;           // log2 units
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;       // 2 stages
+constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;   // 2 stages
+constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;   // 2 buffers
+constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+struct PfBars {
+  uint64_t q_full;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t kv_mask[2];
+  int abort_flag;
+};
+constexpr uint32_t kPfSmemBytes = kOffBar + sizeof(PfBars) + 1024;  // + alignment slack
+
+struct PrefillArgs {
+  void* out;
+  int out_dtype;
+  const int32_t* cu_q_lens;
+  const int32_t* ctx_before;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  int num_heads;
+  int block_size;
+  int num_blocks;
+  int rows_per_load;  // min(block_size, 128)
+  float qscale;       // scale * log2(e)
+  uint32_t idesc_s;   // instruction descriptors
+  uint32_t idesc_pv;
+  int32_t* err_flag;
+};
+
+// ---- tcgen05 / TMA helpers ------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // version
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.  The load and its
+// wait sit in one asm statement, so no use of the registers can be scheduled
+// before the data has arrived.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
+      "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
+      "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
+      "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
+// 128-byte-swizzled [rows][64] half tile.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
+  return (uint32_t)row * 128u + (uint32_t)((chunk ^ (row & 7)) << 4);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+  extern __shared__ uint8_t pf_smem_raw[];
+  const uint32_t raw = smem_u32(pf_smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = pf_smem_raw + (base - raw);
+  PfBars& bars = *reinterpret_cast<PfBars*>(gbase + kOffBar);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // later tiles (more keys) start first
+  const int h = blockIdx.y;
+  const int c = blockIdx.z;
+  const int H = a.num_heads;
+  const int B = a.block_size;
+
+  const int q0 = __ldg(a.cu_q_lens + c);
+  const int n_c = __ldg(a.cu_q_lens + c + 1) - q0;
+  if (qt * kPfRows >= n_c) return;  // uniform across the CTA
+  const int c0 = __ldg(a.ctx_before + c);
+  const int ctx_total = c0 + n_c;
+  if (c0 < 0 || n_c < 0 || (int64_t)ctx_total > (int64_t)a.max_blocks_per_seq * B) {
+    if (threadIdx.x == 0) atomicOr(a.err_flag, PA_FLAG_BAD_LENGTH);
+    return;
+  }
+  const int last_row = min(qt * kPfRows + kPfRows - 1, n_c - 1);
+  const int n_kv = (c0 + last_row) / kPfKeys + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.kv_full[i], 1);
+      mbar_init(&bars.kv_empty[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_empty[i], 4);
+      mbar_init(&bars.p_full[i], 4);
+      mbar_init(&bars.pv_done[i], 1);
+    }
+    mbar_init(&bars.drain, 1);
+    bars.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort_flag;
+
+  if (warp == kPfLoadWarp) {
+    // ---------------------------------------------------------------- loader
+    const int rpl = a.rows_per_load;
+    const int loads = kPfKeys / rpl;  // sub-blocks per key tile (1..8)
+    const int32_t* trow = a.block_tables + (size_t)c * a.max_blocks_per_seq;
+    int issued = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
+      tma_load_3d(base + kOffQ, &tm_q, 0, h, q0 + qt * kPfRows, &bars.q_full);
+      tma_load_3d(base + kOffQ + kHalfBytes, &tm_q, 64, h, q0 + qt * kPfRows, &bars.q_full);
+    }
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&bars.kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, a.err_flag);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int key0 = j * kPfKeys;
+      int row = 0;
+      bool have = false;
+      if (lane < loads) {
+        const int pos = key0 + lane * rpl;
+        if (pos < ctx_total) {
+          const int32_t blk = __ldg(trow + pos / B);
+          if (blk >= 0 && blk < a.num_blocks) {
+            have = true;
+            row = (blk * H + h) * B + pos % B;
+          } else {
+            atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
+          }
+        }
+      }
+      const uint32_t mask = __ballot_sync(0xffffffffu, have);
+      if (lane == 0) {
+        bars.kv_mask[st] = mask;
+        const uint32_t bytes = (uint32_t)__popc(mask) * (uint32_t)rpl * 128u * 4u;
+        mbar_arrive_expect_tx(&bars.kv_full[st], bytes);
+      }
+      for (int r = 0; r < loads; ++r) {
+        const int rr = __shfl_sync(0xffffffffu, row, r);
+        if (lane == 0 && ((mask >> r) & 1u)) {
+          const uint32_t off = (uint32_t)r * rpl * 128u;
+          const uint32_t kdst = base + kOffK + st * kTileBytes + off;
+          const uint32_t vdst = base + kOffV + st * kTileBytes + off;
+          tma_load_2d(kdst, &tm_k, 0, rr, &bars.kv_full[st]);
+          tma_load_2d(kdst + kHalfBytes, &tm_k, 64, rr, &bars.kv_full[st]);
+          tma_load_2d(vdst, &tm_v, 0, rr, &bars.kv_full[st]);
+          tma_load_2d(vdst + kHalfBytes, &tm_v, 64, rr, &bars.kv_full[st]);
+        }
+      }
+      ++issued;
+    }
+    if (lane == 0 && *abort_flag) {  // let in-flight tiles land before exit
+      mbar_wait_drain(&bars.q_full, 0);
+      for (int jj = max(0, issued - 2); jj < issued; ++jj) mbar_wait_drain(&bars.kv_full[jj & 1], (jj >> 1) & 1);
+    }
+  } else if (warp == kPfMmaWarp) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      bool ok = mbar_wait(&bars.q_full, 0, abort_flag, a.err_flag);
+      for (int j = 0; ok && j <= n_kv; ++j) {
+        if (j < n_kv) {
+          const int st = j & 1;
+          ok = mbar_wait(&bars.kv_full[st], (j >> 1) & 1, abort_flag, a.err_flag) &&
+               mbar_wait(&bars.s_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, a.err_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kb = base + kOffK + st * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            umma_f16(tmem + (st ? kTmemS1 : kTmemS0), smem_desc_sw128(base + kOffQ + koff, 16, 1024),
+                     smem_desc_sw128(kb + koff, 16, 1024), a.idesc_s, kk > 0);
+          }
+          umma_commit(&bars.s_full[st]);
+        }
+        if (j >= 1) {
+          const int jj = j - 1;
+          const int st = jj & 1;
+          ok = mbar_wait(&bars.p_full[st], (jj >> 1) & 1, abort_flag, a.err_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t pb = base + kOffP + st * kTileBytes;
+          const uint32_t vb = base + kOffV + st * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t poff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            umma_f16(tmem + kTmemO, smem_desc_sw128(pb + poff, 16, 1024),
+                     smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), a.idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars.pv_done[st]);
+          umma_commit(&bars.kv_empty[st]);
+        }
+      }
+      // every issued MMA has finished before tensor memory is released
+      umma_commit(&bars.drain);
+      mbar_wait_drain(&bars.drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax warps 0-3
+    const int row = threadIdx.x;  // query row within the tile = TMEM lane
+    const int qrow = qt * kPfRows + row;
+    const int pos = c0 + qrow;
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const int rpl = a.rows_per_load;
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      // kv_full: the loader's mask for this tile and the V rows are read below
+      ok = mbar_wait(&bars.s_full[st], (j >> 1) & 1, abort_flag, a.err_flag) &&
+           mbar_wait(&bars.kv_full[st], (j >> 1) & 1, abort_flag, a.err_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kPfKeys];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(lane_addr + (st ? kTmemS1 : kTmemS0) + cc * 32, s + cc * 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_empty[st]);
+
+      const int key0 = j * kPfKeys;
+      const uint32_t kmask = bars.kv_mask[st];
+      const int lim = min(pos, ctx_total - 1) - key0;  // last admissible column
+      float rmax = -INFINITY;
+#pragma unroll
+      for (int col = 0; col < kPfKeys; ++col) {
+        const bool valid = col <= lim && ((kmask >> (col / rpl)) & 1u);
+        s[col] = valid ? s[col] * a.qscale : -INFINITY;
+        rmax = fmaxf(rmax, s[col]);
+      }
+      const float m_new = fmaxf(m_used, rmax);
+      const bool resc = m_new > m_used + kRescaleThreshold;  // also true when m_used is -inf
+      const float m_next = resc ? m_new : m_used;
+      const float alpha = resc ? ((m_used == -INFINITY) ? 0.f : exp2f(m_used - m_next)) : 1.f;
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled
+        ok = mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, a.err_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(lane_addr + kTmemO + cc * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(lane_addr + kTmemO + cc * 32, o);
+        }
+        tmem_st_wait();
+      }
+      l *= alpha;
+      const float mref = (m_next == -INFINITY) ? 0.f : m_next;
+#pragma unroll
+      for (int col = 0; col < kPfKeys; ++col) {
+        s[col] = exp2f(s[col] - mref);
+        l += s[col];
+      }
+      // the P buffer of this stage was last read by P_{j-2} V_{j-2}
+      if (j >= 2) {
+        ok = mbar_wait(&bars.pv_done[st], ((j - 2) >> 1) & 1, abort_flag, a.err_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      }
+      uint8_t* pbuf = gbase + kOffP + st * kTileBytes;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const float* src = s + half * 64 + ch * 8;
+          uint4 v;
+          v.x = pack2<T>(src[0], src[1]);
+          v.y = pack2<T>(src[2], src[3]);
+          v.z = pack2<T>(src[4], src[5]);
+          v.w = pack2<T>(src[6], src[7]);
+          *reinterpret_cast<uint4*>(pbuf + half * kHalfBytes + sw128_offset(row, ch)) = v;
+        }
+      }
+      // key row `row` of V: zero it if it was not loaded or lies past the context
+      const int key = key0 + row;
+      if (key >= ctx_total || !((kmask >> (row / rpl)) & 1u)) {
+        uint8_t* vbuf = gbase + kOffV + st * kTileBytes;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          *reinterpret_cast<uint4*>(vbuf + row * 128 + ch * 16) = z;
+          *reinterpret_cast<uint4*>(vbuf + kHalfBytes + row * 128 + ch * 16) = z;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full[st]);
+      m_used = m_next;
+    }
+    if (ok) {
+      const int jl = n_kv - 1;
+      ok = mbar_wait(&bars.pv_done[jl & 1], (jl >> 1) & 1, abort_flag, a.err_flag);
+    }
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = qrow < n_c;
+      const size_t obase = ((size_t)(q0 + qrow) * H + h) * kPfD;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float o[32];
+        tmem_ld32(lane_addr + kTmemO + cc * 32, o);
+        if (store) {
+          if (a.out_dtype == PA_F32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + obase + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + obase + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float* x = o + 8 * i;
+              uint4 v;
+              if (a.out_dtype == PA_BF16) {
+                v.x = pack2<__nv_bfloat16>(x[0] * inv, x[1] * inv);
+                v.y = pack2<__nv_bfloat16>(x[2] * inv, x[3] * inv);
+                v.z = pack2<__nv_bfloat16>(x[4] * inv, x[5] * inv);
+                v.w = pack2<__nv_bfloat16>(x[6] * inv, x[7] * inv);
+              } else {
+                v.x = pack2<__half>(x[0] * inv, x[1] * inv);
+                v.y = pack2<__half>(x[2] * inv, x[3] * inv);
+                v.z = pack2<__half>(x[4] * inv, x[5] * inv);
+                v.w = pack2<__half>(x[6] * inv, x[7] * inv);
+              }
+              dst[i] = v;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace pa
+
+// ---------------------------------------------------------------------------------
+// Host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A/B in
+// `ab_format` (0 = fp16, 1 = bf16), M = 128, N = 128, B K-major or MN-major.
+uint32_t make_idesc(uint32_t ab_format, bool b_mn_major) {
+  uint32_t d = 0;
+  d |= 1u << 4;                 // D format: f32
+  d |= ab_format << 7;          // A format
+  d |= ab_format << 10;         // B format
+  d |= (b_mn_major ? 1u : 0u) << 16;
+  d |= (uint32_t)(128 >> 3) << 17;  // N
+  d |= (uint32_t)(128 >> 4) << 24;  // M
+  return d;
+}
+
+}  // namespace
+
+extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens,
+                                const int32_t* ctx_before, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, int max_blocks_per_seq, int num_chunks, int total_q,
+                                int max_q_len, int num_heads, int head_dim, int block_size, int num_blocks,
+                                float scale, int dtype, int32_t* err_flag, void* stream) {
+  if (!pa_host::is_kv_dtype(dtype) || !pa_host::is_out_dtype(out_dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size <= 0 || block_size % 16 != 0 || !(128 % block_size == 0 || block_size % 128 == 0))
+    return PA_ERR_UNSUPPORTED;
+  if (num_chunks < 0 || total_q < 0 || max_q_len < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_chunks == 0 || total_q == 0 || max_q_len == 0) return PA_OK;
+  if (num_chunks > 65535 || num_heads > 65535) return PA_ERR_INVALID_ARG;
+  if (!out || !q || !cu_q_lens || !ctx_before || !k_pool || !v_pool || !block_tables || !err_flag)
+    return PA_ERR_INVALID_ARG;
+  if (!pa_host::aligned16(q) || !pa_host::aligned16(k_pool) || !pa_host::aligned16(v_pool) ||
+      !pa_host::aligned16(out))
+    return PA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID_ARG;
+  const uint64_t pool_rows = (uint64_t)num_blocks * num_heads * block_size;
+  if (pool_rows >= (1ull << 31)) return PA_ERR_INVALID_ARG;
+
+  auto encode = get_encode_fn();
+  if (encode == nullptr) return PA_ERR_CUDA;
+  const CUtensorMapDataType tdt = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    cuuint64_t dims[3] = {128, (cuuint64_t)num_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)num_heads * 128 * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&tm_q, tdt, 3, const_cast<void*>(q), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PA_ERR_CUDA;
+  }
+  const int rows_per_load = block_size < 128 ? block_size : 128;
+  for (int which = 0; which < 2; ++which) {
+    cuuint64_t dims[2] = {128, (cuuint64_t)pool_rows};
+    cuuint64_t strides[1] = {128 * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)rows_per_load};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(which ? &tm_v : &tm_k, tdt, 2, const_cast<void*>(which ? v_pool : k_pool), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PA_ERR_CUDA;
+  }
+
+  pa::PrefillArgs a;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.cu_q_lens = cu_q_lens;
+  a.ctx_before = ctx_before;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_heads = num_heads;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.rows_per_load = rows_per_load;
+  a.qscale = scale * 1.4426950408889634f;
+  const uint32_t fmt = dtype == PA_BF16 ? 1u : 0u;
+  a.idesc_s = make_idesc(fmt, false);
+  a.idesc_pv = make_idesc(fmt, true);
+  a.err_flag = err_flag;
+
+  auto kern = dtype == PA_BF16 ? pa::prefill_kernel<__nv_bfloat16> : pa::prefill_kernel<__half>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  static int configured[2][64] = {{0}};
+  if (!configured[fmt][dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pa::kPfSmemBytes) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    configured[fmt][dev] = 1;
+  }
+  dim3 grid((max_q_len + pa::kPfRows - 1) / pa::kPfRows, num_heads, num_chunks);
+  kern<<<grid, pa::kPfThreads, pa::kPfSmemBytes, (cudaStream_t)stream>>>(tm_q, tm_k, tm_v, a);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

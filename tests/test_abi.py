@@ -1,0 +1,209 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library loads, exports every function include/pa.h declares, rejects
+bad arguments before launching anything, and its host block allocator and
+slot helper agree operation by operation with the oracle's model.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.alloc_model import BlockAllocatorModel
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_35_gb300 as pa
+
+    return pa
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(pa):
+    names = header_functions()
+    assert len(names) >= 20
+    L = ctypes.CDLL(pa.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(pa.SIGNATURES) == names
+
+
+def test_status_strings_and_version(pa):
+    assert pa.lib().pa_version() >= 100
+    for st in range(9):
+        assert pa.status_string(st) not in ("", "unknown status")
+    assert pa.status_string(99) == "unknown status"
+
+
+def test_bad_arguments_are_rejected_before_launch(pa):
+    L = pa.lib()
+    fake = ctypes.c_void_p(0x1000)
+    # unsupported head_dim / block size / dtype
+    args = [fake, pa.PA_F16, fake, fake, fake, fake, 4, fake, 64, 2, 4, 96, 16, 8, 0.1, pa.PA_F16, fake, 1 << 20, 0,
+            fake, None]
+    assert L.pa_decode(*args) == pa.PA_ERR_UNSUPPORTED
+    args[11] = 128
+    args[12] = 24
+    assert L.pa_decode(*args) == pa.PA_ERR_UNSUPPORTED
+    args[12] = 16
+    args[15] = 7
+    assert L.pa_decode(*args) == pa.PA_ERR_UNSUPPORTED
+    args[15] = pa.PA_F16
+    args[17] = 16  # workspace too small
+    assert L.pa_decode(*args) == pa.PA_ERR_WORKSPACE
+    args[17] = 1 << 20
+    args[18] = 24  # partition not a multiple of 16
+    assert L.pa_decode(*args) == pa.PA_ERR_INVALID_ARG
+    args[18] = 0
+    args[16] = None
+    assert L.pa_decode(*args) == pa.PA_ERR_INVALID_ARG
+    args[9] = 0  # no sequences: nothing to do
+    assert L.pa_decode(*args) == pa.PA_OK
+    # prefill: head_dim 64 unsupported, block size 48 unsupported
+    pargs = [fake, pa.PA_BF16, fake, fake, fake, fake, fake, fake, 8, 2, 100, 64, 4, 64, 16, 8, 0.1, pa.PA_BF16, fake,
+             None]
+    assert L.pa_prefill_chunk(*pargs) == pa.PA_ERR_UNSUPPORTED
+    pargs[13] = 128
+    pargs[14] = 48
+    assert L.pa_prefill_chunk(*pargs) == pa.PA_ERR_UNSUPPORTED
+    # scatter / copy with nothing to do
+    assert L.pa_reshape_and_cache(fake, fake, fake, fake, fake, 0, 4, 64, 16, 8, pa.PA_F16, fake, None) == pa.PA_OK
+    assert L.pa_copy_blocks(fake, fake, fake, 0, 4, 64, 16, 8, pa.PA_F16, fake, None) == pa.PA_OK
+    assert L.pa_copy_blocks(fake, fake, fake, 1, 4, 64, 16, 8, 9, fake, None) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_get_error(None, None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_partition_and_workspace_sizes(pa):
+    assert pa.pa_decode_partition_size(64, 40, 2048) == 512
+    assert pa.pa_decode_partition_size(256, 32, 16384) == 512
+    P = pa.pa_decode_partition_size(1, 8, 4096)
+    assert 64 <= P <= 512 and P % 16 == 0
+    for S, H, D, mx in ((64, 40, 128, 2048), (256, 32, 128, 16384), (4, 4, 64, 46)):
+        n = pa.pa_decode_workspace_bytes(S, H, D, mx, 0)
+        P = pa.pa_decode_partition_size(S, H, mx)
+        parts = -(-mx // P)
+        assert n >= 4 * S * H * parts * (D + 2) and n % 256 == 0
+    assert pa.pa_decode_workspace_bytes(4, 4, 64, 100, 24) == 0
+    assert pa.pa_decode_workspace_bytes(4, 4, 64, 100, 2048) == 0
+
+
+def test_slot_mapping_matches_the_oracle(pa):
+    rng = np.random.default_rng(0)
+    for B in (16, 256):
+        tables = rng.permutation(400)[:120].reshape(6, 20).astype(np.int32)
+        seq = rng.integers(0, 6, 300).astype(np.int32)
+        pos = rng.integers(0, 20 * B, 300).astype(np.int32)
+        got = pa.pa_slot_mapping(tables, seq, pos, B)
+        want = [oracle.slot_of(tables[s], int(p), B) for s, p in zip(seq, pos)]
+        assert got.tolist() == want
+    tables = np.array([[3, -1]], dtype=np.int32)
+    with pytest.raises(pa.PAError):
+        pa.pa_slot_mapping(tables, [0], [16], 16)
+
+
+def _compare(model: BlockAllocatorModel, alloc, seq_ids):
+    assert alloc.num_free() == model.num_free()
+    assert alloc.num_seqs() == len(model.seqs)
+    for b in range(model.num_blocks):
+        assert alloc.ref(b) == model.ref[b]
+    for s in seq_ids:
+        if s in model.seqs:
+            tbl, ln = alloc.block_table(s)
+            assert tbl == model.table(s) and ln == model.length(s)
+
+
+def test_allocator_matches_model_on_random_operations(pa):
+    rng = random.Random(1)
+    for trial in range(12):
+        N = rng.randint(4, 48)
+        B = rng.choice([1, 4, 16, 256])
+        model = BlockAllocatorModel(N, B)
+        alloc = pa.BlockAllocator(N, B)
+        nxt = 0
+        for _ in range(250):
+            live = list(model.seqs)
+            op = rng.random()
+            if op < 0.15 or not live:
+                model.add_seq(nxt)
+                alloc.add_seq(nxt)
+                nxt += 1
+            elif op < 0.25:
+                p = rng.choice(live)
+                model.fork(p, nxt)
+                alloc.fork(p, nxt)
+                nxt += 1
+            elif op < 0.33:
+                s = rng.choice(live)
+                model.free_seq(s)
+                alloc.free_seq(s)
+            else:
+                batch = rng.sample(live, rng.randint(1, len(live)))
+                try:
+                    want_slots, want_pairs = model.append_slots(batch)
+                except MemoryError:
+                    with pytest.raises(pa.PAError) as ei:
+                        alloc.append_slots(batch)
+                    assert ei.value.status == pa.PA_ERR_NO_FREE_BLOCKS
+                else:
+                    slots, pairs = alloc.append_slots(batch)
+                    assert slots.tolist() == want_slots
+                    assert [tuple(p) for p in pairs.tolist()] == want_pairs
+            _compare(model, alloc, range(nxt))
+        alloc.close()
+
+
+def test_allocator_errors(pa):
+    a = pa.BlockAllocator(2, 4)
+    a.add_seq(0)
+    with pytest.raises(pa.PAError):
+        a.add_seq(0)
+    with pytest.raises(pa.PAError):
+        a.fork(5, 6)
+    with pytest.raises(pa.PAError):
+        a.append_slots([0, 0])
+    a.add_seq(1)
+    a.add_seq(2)
+    a.append_slots([0, 1])
+    with pytest.raises(pa.PAError) as ei:
+        a.append_slots([2])
+    assert ei.value.status == pa.PA_ERR_NO_FREE_BLOCKS
+    assert a.block_table(2) == ([], 0)
+    tables, lens = a.block_tables([0, 1, 2], 3)
+    assert tables[2].tolist() == [-1, -1, -1] and lens.tolist() == [1, 1, 0]
+    assert a.ref(-1) == -1 and a.ref(2) == -1
+
+
+def test_shared_prefix_copy_pairs_match_model(pa):
+    """The 8-sample shared-prompt flow: 7 copy pairs, the 8th writes in place."""
+    B = 16
+    model = BlockAllocatorModel(200, B)
+    alloc = pa.BlockAllocator(200, B)
+    for m in (model, alloc):
+        m.add_seq(0)
+    for _ in range(1000):
+        model.append_slots([0])
+        alloc.append_slots([0])
+    for c in range(1, 8):
+        model.fork(0, c)
+        alloc.fork(0, c)
+    ws, wp = model.append_slots(list(range(8)))
+    gs, gp = alloc.append_slots(list(range(8)))
+    assert gs.tolist() == ws and [tuple(p) for p in gp.tolist()] == wp and len(wp) == 7
+    _compare(model, alloc, range(8))

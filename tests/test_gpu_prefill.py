@@ -1,0 +1,117 @@
+"""GPU parity of the tcgen05 chunked-prefill kernel against the CPU oracle."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pa_workloads as W
+from tests.gpu_common import TORCH_OUT, assert_attn_close, oracle_slots
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_35_gb300 as pa
+
+    torch.cuda.set_device(0)
+    return pa
+
+
+def chunk_positions(m):
+    seq_idx = np.concatenate([np.full(n, c) for c, n in enumerate(m.chunk_lens.tolist())])
+    pos = np.concatenate([np.arange(c0, c0 + n) for c0, n in zip(m.ctx_before.tolist(), m.chunk_lens.tolist())])
+    return seq_idx, pos
+
+
+def cu_lens(m):
+    return torch.cat([torch.zeros(1, dtype=torch.int32), m.chunk_lens.cumsum(0).to(torch.int32)])
+
+
+def run_prefill(pa, m, out_dtype="f32", tables=None):
+    """Write the chunks' K/V with pa_reshape_and_cache, then pa_prefill_chunk."""
+    w = m.decode
+    dev = torch.device("cuda")
+    kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
+    tables = m.chunk_tables if tables is None else tables
+    seq_idx, pos = chunk_positions(m)
+    slots = pa.pa_slot_mapping(m.chunk_tables, seq_idx, pos, w.block_size)
+    err = pa.new_error_flag()
+    pa.pa_reshape_and_cache(m.chunk_k.to(dev), m.chunk_v.to(dev), kp, vp, torch.from_numpy(slots).to(dev), err)
+    assert pa.pa_get_error(err) == 0
+    T = int(m.chunk_lens.sum())
+    out = torch.full((T, w.num_heads, w.head_dim), float("nan"), dtype=TORCH_OUT[out_dtype], device=dev)
+    pa.pa_prefill_chunk(out, m.chunk_q.to(dev), cu_lens(m).to(dev), m.ctx_before.to(dev), kp, vp, tables.to(dev),
+                        int(m.chunk_lens.max()), w.scale, err)
+    flags = pa.pa_get_error(err)
+    return out, flags, kp, vp
+
+
+def oracle_prefill(m):
+    w = m.decode
+    kb, vb = oracle.pool_bits(w.k_pool), oracle.pool_bits(w.v_pool)
+    seq_idx, pos = chunk_positions(m)
+    oracle.reshape_and_cache(m.chunk_k, m.chunk_v, kb, vb, oracle_slots(m.chunk_tables, seq_idx, pos, w.block_size),
+                             w.block_size)
+    ref = oracle.prefill(m.chunk_q, cu_lens(m), m.ctx_before, kb, vb, m.chunk_tables, w.block_size, w.scale, w.dtype)
+    return ref, kb, vb
+
+
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_prefill_small_ragged_bf16(pa, out_dtype):
+    m = W.small_prefill()
+    out, flags, _, _ = run_prefill(pa, m, out_dtype)
+    assert flags == 0
+    ref, _, _ = oracle_prefill(m)
+    assert_attn_close(out, ref, out_dtype, "prefill bf16")
+
+
+@pytest.mark.parametrize("B", [16, 32, 128, 256])
+def test_prefill_block_sizes(pa, B):
+    m = W.small_prefill(chunk_lens=(200, 64), ctx_before=(300, 0), H=2, B=B)
+    out, flags, _, _ = run_prefill(pa, m, "f32")
+    assert flags == 0
+    ref, _, _ = oracle_prefill(m)
+    assert_attn_close(out, ref, "f32", f"prefill block {B}")
+
+
+def test_prefill_fp16_tile_aligned_chunks(pa):
+    m = W.small_prefill(chunk_lens=(128, 256, 1), ctx_before=(128, 0, 511), H=2, B=16, dtype="f16")
+    out, flags, _, _ = run_prefill(pa, m, "f16")
+    assert flags == 0
+    ref, _, _ = oracle_prefill(m)
+    assert_attn_close(out, ref, "f16", "prefill fp16")
+
+
+def test_prefill_rows_match_decode_at_their_positions(pa):
+    """Cross-kernel: chunk row i equals pa_decode of the same query with a
+    context of ctx_before + i + 1 tokens."""
+    m = W.small_prefill(chunk_lens=(150,), ctx_before=(333,), H=2, B=16)
+    out, flags, kp, vp = run_prefill(pa, m, "f32")
+    assert flags == 0
+    w = m.decode
+    rows = torch.arange(0, 150, 7)
+    ctx = (m.ctx_before[0] + rows + 1).to(torch.int32)
+    tables = m.chunk_tables.expand(len(rows), -1).contiguous()
+    q = m.chunk_q[rows].contiguous()
+    dev = torch.device("cuda")
+    dout = torch.empty(len(rows), w.num_heads, w.head_dim, dtype=torch.float32, device=dev)
+    ws = pa.decode_workspace(len(rows), w.num_heads, w.head_dim, int(ctx.max()))
+    err = pa.new_error_flag()
+    pa.pa_decode(dout, q.to(dev), kp, vp, tables.to(dev), ctx.to(dev), int(ctx.max()), w.scale, ws, err)
+    assert pa.pa_get_error(err) == 0
+    assert float((dout.cpu() - out[rows].cpu()).abs().max()) <= 2e-3
+
+
+def test_prefill_flags_bad_table_entry(pa):
+    m = W.small_prefill(chunk_lens=(40,), ctx_before=(100,), H=1, B=16)
+    bad = m.chunk_tables.clone()
+    bad[0, 2] = -3
+    out, flags, _, _ = run_prefill(pa, m, "f32", tables=bad)
+    assert flags == pa.PA_FLAG_BAD_BLOCK
+    assert torch.isfinite(out).all()

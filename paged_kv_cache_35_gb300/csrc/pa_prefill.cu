@@ -19,7 +19,12 @@
 //      warps 0-3 (softmax) thread i owns query row i = TMEM lane i: it reads
 //              its score row with tcgen05.ld, applies the causal / context
 //              mask, runs the online softmax, and writes its probability row
-//              as bf16/fp16 into a shared-memory operand for the P V product.
+//              into a shared-memory operand for the P V product as two
+//              16-bit parts, P = P_hi + P_lo (P_hi = P rounded to the input
+//              type, P_lo = the rounded remainder), and O += P_hi V + P_lo V.
+//              One 16-bit P would carry only 8 (bf16) or 11 (fp16) bits and
+//              its rounding alone moves a peaked row's output by ~2^-9 |v|;
+//              the two parts carry ~16 bits, at the cost of one more MMA group.
 //    S_{j+1} is issued before P_j V_j, so the softmax of tile j+1 overlaps
 //    the tensor-core work of tile j.
 //  * Operands are 128-byte-swizzled: K-major for Q, K and P; V is consumed
@@ -57,7 +62,7 @@ constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;       // 2 stages
 constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;   // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;   // 2 buffers
+constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;   // P_hi, then P_lo
 constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
 struct PfBars {
   uint64_t q_full;
@@ -182,6 +187,18 @@ template <>
 __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// x rounded (to nearest even) to the 16-bit type T, returned as float.
+template <typename T>
+__device__ __forceinline__ float round_to(float x);
+template <>
+__device__ __forceinline__ float round_to<__half>(float x) {
+  return __half2float(__float2half_rn(x));
+}
+template <>
+__device__ __forceinline__ float round_to<__nv_bfloat16>(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
@@ -327,13 +344,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ok = mbar_wait(&bars.p_full[st], (jj >> 1) & 1, abort_flag, a.err_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t pb = base + kOffP + st * kTileBytes;
           const uint32_t vb = base + kOffV + st * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t poff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            umma_f16(tmem + kTmemO, smem_desc_sw128(pb + poff, 16, 1024),
-                     smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), a.idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          for (int part = 0; part < 2; ++part) {  // P_hi V, then P_lo V
+            const uint32_t pb = base + kOffP + part * kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t poff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+              umma_f16(tmem + kTmemO, smem_desc_sw128(pb + poff, 16, 1024),
+                       smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), a.idesc_pv,
+                       (jj > 0 || kk > 0 || part > 0) ? 1u : 0u);
+            }
           }
           umma_commit(&bars.pv_done[st]);
           umma_commit(&bars.kv_empty[st]);
@@ -384,24 +405,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool resc = m_new > m_used + kRescaleThreshold;  // also true when m_used is -inf
       const float m_next = resc ? m_new : m_used;
       const float alpha = resc ? ((m_used == -INFINITY) ? 0.f : exp2f(m_used - m_next)) : 1.f;
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        // O must hold P_{j-1} V_{j-1} before it is rescaled
-        ok = mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, a.err_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
-          tmem_ld32(lane_addr + kTmemO + cc * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(lane_addr + kTmemO + cc * 32, o);
-        }
-        tmem_st_wait();
-      }
       l *= alpha;
       const float mref = (m_next == -INFINITY) ? 0.f : m_next;
 #pragma unroll
@@ -409,26 +412,52 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         s[col] = exp2f(s[col] - mref);
         l += s[col];
       }
-      // the P buffer of this stage was last read by P_{j-2} V_{j-2}
-      if (j >= 2) {
-        ok = mbar_wait(&bars.pv_done[st], ((j - 2) >> 1) & 1, abort_flag, a.err_flag);
+      // P_{j-1} V_{j-1} must be complete: it reads the P buffer written below
+      // and it is the last product O holds before a rescale
+      if (j > 0) {
+        ok = mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, a.err_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            tmem_ld32(lane_addr + kTmemO + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_addr + kTmemO + cc * 32, o);
+          }
+          tmem_st_wait();
+        }
       }
-      uint8_t* pbuf = gbase + kOffP + st * kTileBytes;
+      uint8_t* phi = gbase + kOffP;
+      uint8_t* plo = gbase + kOffP + kTileBytes;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const float* src = s + half * 64 + ch * 8;
-          uint4 v;
-          v.x = pack2<T>(src[0], src[1]);
-          v.y = pack2<T>(src[2], src[3]);
-          v.z = pack2<T>(src[4], src[5]);
-          v.w = pack2<T>(src[6], src[7]);
-          *reinterpret_cast<uint4*>(pbuf + half * kHalfBytes + sw128_offset(row, ch)) = v;
+          float hi[8], lo[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            hi[e] = round_to<T>(src[e]);
+            lo[e] = src[e] - hi[e];
+          }
+          uint4 vh, vl;
+          vh.x = pack2<T>(hi[0], hi[1]);
+          vh.y = pack2<T>(hi[2], hi[3]);
+          vh.z = pack2<T>(hi[4], hi[5]);
+          vh.w = pack2<T>(hi[6], hi[7]);
+          vl.x = pack2<T>(lo[0], lo[1]);
+          vl.y = pack2<T>(lo[2], lo[3]);
+          vl.z = pack2<T>(lo[4], lo[5]);
+          vl.w = pack2<T>(lo[6], lo[7]);
+          const uint32_t off = half * kHalfBytes + sw128_offset(row, ch);
+          *reinterpret_cast<uint4*>(phi + off) = vh;
+          *reinterpret_cast<uint4*>(plo + off) = vl;
         }
       }
       // key row `row` of V: zero it if it was not loaded or lies past the context

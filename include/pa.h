@@ -127,8 +127,9 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
  *     x_j = scale * q[s][h] . K_s[j],  j in [0, n), K_s[j] = K_pool[table[s][j/B]][h][j%B]
  *     out[s][h] = sum_j softmax(x)_j V_s[j]
  * computed block by block with an online softmax inside each split-KV
- * partition of `partition_size` tokens and a log-sum-exp combine of the
- * partitions.  n == 0 gives a zero row.
+ * partition and a log-sum-exp combine of the partitions (in token order, so
+ * the result is deterministic).  A sequence is cut into partitions of
+ * `partition_size` tokens (the last one partial).  n == 0 gives a zero row.
  * q: device [num_seqs][num_heads][head_dim], dtype `dtype`.
  * out: device [num_seqs][num_heads][head_dim], dtype `out_dtype`.
  * context_lens: device int32 [num_seqs], each <= max_context_len and

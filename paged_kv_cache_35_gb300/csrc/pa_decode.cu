@@ -17,24 +17,30 @@
 //  * The decode kernel is persistent (SM count x resident CTAs) and warp
 //    specialised:
 //      warp 5  (scheduler) takes unit ids from a global counter, reads the
-//              item, the context length and the table entries of the unit
-//              into a 4-deep unit queue in shared memory, and bulk-copies
-//              the unit's query row next to them;
+//              item and the table entries of the unit into a 4-deep unit
+//              queue in shared memory, bulk-copies the unit's query row next
+//              to them, and merges each finished unit;
 //      warp 4  (producer)  streams the unit's 16-token K and V tiles (one
 //              contiguous 16*D*2-byte run each in the [NB][H][B][D] pools)
-//              into an 8-stage shared-memory ring with cp.async.bulk,
-//              completion counted in bytes on one mbarrier per stage;
+//              into shared-memory ring slots with cp.async.bulk, completion
+//              counted in bytes on one mbarrier per slot; tile j of a unit
+//              goes to consumer warp j % 4, into that warp's own slots;
 //      warps 0-3 (consumers) take every 4th tile of the unit: 8 lanes per
 //              token row, 16-byte shared loads (conflict free), fp32 dot
 //              products reduced with 3 shuffles, online softmax (running max
 //              and sum, base-2 exponent with log2(e) folded into the query).
-//    The four consumer warps merge their (max, sum, output) through shared
-//    memory; a unit that is the only partition of its sequence writes the
-//    output directly.  Otherwise it writes its normalised partial and
-//    (max, sum) to the workspace, and the warp that completes the last
-//    partition of a (sequence, head) merges all partitions with the
-//    log-sum-exp rule in partition order (so the result does not depend on
-//    scheduling, nor on which physical blocks hold the tokens).
+//    Each consumer warp leaves its (max, sum, output) for the unit in shared
+//    memory and goes on to the next unit at once; the scheduler warp merges
+//    the four shares (so no streaming warp ever waits on a merge).  A unit
+//    that is the only partition of its sequence writes the output directly.
+//    Otherwise the scheduler writes the normalised partial and (max, sum) to
+//    the workspace, and the one that completes the last partition of a
+//    (sequence, head) merges all partitions with the log-sum-exp rule in
+//    partition order (so the result does not depend on scheduling, nor on
+//    which physical blocks hold the tokens).
+//  * Each CTA's first unit is its own index (no counter round trip at start);
+//    the work items carry their token count and partition count, so the
+//    scheduler's chain is counter -> item -> table entries.
 //  * Every wait is bounded; bad table entries are flagged, never trapped.
 #include <math.h>
 
@@ -42,16 +48,32 @@
 
 namespace pa {
 
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 4
+#endif
+#ifndef PA_DECODE_CONSUMER_WARPS
+#define PA_DECODE_CONSUMER_WARPS 4
+#endif
+#ifndef PA_DECODE_MIN_CTAS
+#define PA_DECODE_MIN_CTAS 5
+#endif
+
 constexpr int kChunk = 16;                    // tokens per ring stage
-constexpr int kConsumerWarps = 4;
-constexpr int kProducerWarp = kConsumerWarps;  // warp 4
+constexpr int kConsumerWarps = PA_DECODE_CONSUMER_WARPS;
+constexpr int kProducerWarp = kConsumerWarps;  // the warp after the consumers
 constexpr int kSchedulerWarp = kConsumerWarps + 1;
 constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;
-constexpr int kStages = 8;
+constexpr int kStages = PA_DECODE_STAGES;
+// Each consumer warp owns its own kSlotsPerWarp ring slots and consumes them
+// strictly in order, so every waiter on a slot's mbarrier observes every
+// phase of it: a parity wait can never alias a phase two ahead.
+constexpr int kSlotsPerWarp = kStages / kConsumerWarps;
+static_assert(kStages % kConsumerWarps == 0, "ring slots must split evenly over the consumer warps");
 constexpr int kUnitQueue = 4;
 constexpr int kMaxPartition = 1024;
 constexpr int kMaxChunksPerUnit = kMaxPartition / kChunk;
 constexpr int kPlanThreads = 1024;
+
 
 struct DecodeArgs {
   void* out;
@@ -71,7 +93,7 @@ struct DecodeArgs {
   int partition_size;
   int max_parts;
   int* counters;   // [0] unit counter, [1] item count, [2 + s*H + h] partition arrivals
-  int2* items;     // (sequence, partition) in processing order
+  int4* items;     // (sequence, partition, first token, tokens | partitions << 11), processing order
   float2* part_ml; // [S][H][max_parts] (max, sum) in log2 units
   float* part_o;   // [S][H][max_parts][D] normalised partial outputs
   int32_t* err_flag;
@@ -82,17 +104,17 @@ struct DecodeSmem {
   T ring[kStages][2][kChunk * D];  // K tile, V tile
   T qbuf[kUnitQueue][D];
   int32_t chunk_blk[kUnitQueue][kMaxChunksPerUnit];
-  int4 unit[kUnitQueue];  // sequence, head, partition, tokens in partition
+  int4 unit[kUnitQueue];  // sequence (< 0: no more units), head, partition, tokens in partition
   int unit_nparts[kUnitQueue];
-  float co[2][kConsumerWarps][D];
-  float cm[2][kConsumerWarps];
-  float cl[2][kConsumerWarps];
+  int unit_tok0[kUnitQueue];
+  float co[kUnitQueue][kConsumerWarps][D];  // each consumer warp's share of a unit
+  float cm[kUnitQueue][kConsumerWarps];
+  float cl[kUnitQueue][kConsumerWarps];
   int slot_ok[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t ufull[kUnitQueue];
-  uint64_t uempty[kUnitQueue];
-  uint64_t comb[2];
+  uint64_t ufull[kUnitQueue];  // unit published: 1 arrival + the query row's bytes
+  uint64_t udone[kUnitQueue];  // every consumer warp has left its share of the unit
   int abort_flag;
 };
 
@@ -121,12 +143,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
   }
   for (int i = tid; i < S * H; i += blockDim.x) a.counters[2 + i] = 0;
   __syncthreads();
+  // item sizes: full partitions of P tokens, then the last part of each
+  // sequence (1..P tokens)
   for (int s = tid; s < S; s += blockDim.x) {
     const int ctx = __ldg(a.context_lens + s);
     if (!length_ok(a, ctx) || ctx == 0) continue;
-    const int np = (ctx + P - 1) / P;
-    const int last = ctx - (np - 1) * P;
-    if (np > 1) atomicAdd(&hist[nb - 1], np - 1);
+    const int nfull = (ctx - 1) / P;
+    const int last = ctx - nfull * P;
+    if (nfull > 0) atomicAdd(&hist[nb - 1], nfull);
     atomicAdd(&hist[(last + kChunk - 1) / kChunk - 1], 1);
   }
   __syncthreads();
@@ -147,14 +171,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
       for (int i = 0; i < H * D; ++i) store_out(a.out, (size_t)s * H * D + i, a.out_dtype, 0.f);
       continue;
     }
-    const int np = (ctx + P - 1) / P;
-    const int last = ctx - (np - 1) * P;
-    if (np > 1) {
-      const int base = offs[nb - 1] + atomicAdd(&cur[nb - 1], np - 1);
-      for (int p = 0; p < np - 1; ++p) a.items[base + p] = make_int2(s, p);
+    const int nfull = (ctx - 1) / P;
+    const int last = ctx - nfull * P;
+    const int nparts = nfull + 1;
+    if (nfull > 0) {
+      const int base = offs[nb - 1] + atomicAdd(&cur[nb - 1], nfull);
+      for (int p = 0; p < nfull; ++p) a.items[base + p] = make_int4(s, p, p * P, P | (nparts << 11));
     }
-    const int lb = (last + kChunk - 1) / kChunk - 1;
-    a.items[offs[lb] + atomicAdd(&cur[lb], 1)] = make_int2(s, np - 1);
+    const int bkt = (last + kChunk - 1) / kChunk - 1;
+    a.items[offs[bkt] + atomicAdd(&cur[bkt], 1)] = make_int4(s, nfull, nfull * P, last | (nparts << 11));
   }
 }
 
@@ -248,53 +273,121 @@ __device__ __forceinline__ void merge_partitions(const DecodeArgs& a, int s, int
   if (lane == 0) a.counters[2 + s * a.num_heads + h] = 0;
 }
 
+// Publish the CTA's k-th unit into queue slot k % kUnitQueue (whole warp).
+// The first unit of every CTA is its own index; later ones come from the
+// global counter.  Returns false when the work is exhausted: a "no more
+// units" marker has been published instead.
+template <int D, typename T>
+__device__ __forceinline__ bool publish_unit(const DecodeArgs& a, DecodeSmem<D, T>& sm, int k,
+                                             long long total_units, int lane) {
+  const int H = a.num_heads;
+  const int qs = k % kUnitQueue;
+  int u = blockIdx.x;
+  if (k > 0) {
+    if (lane == 0) u = (int)gridDim.x + atomicAdd(a.counters, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+  }
+  if ((long long)u >= total_units) {
+    if (lane == 0) {
+      sm.unit[qs] = make_int4(-1, 0, 0, 0);
+      mbar_arrive(&sm.ufull[qs]);
+    }
+    return false;
+  }
+  const int item = u / H;
+  const int h = u - item * H;
+  const int4 it = __ldg(a.items + item);
+  const int s = it.x;
+  const int tok0 = it.z;
+  const int ntok = it.w & 2047;
+  const int nchunks = (ntok + kChunk - 1) / kChunk;
+  const int32_t* trow = a.block_tables + (size_t)s * a.max_blocks_per_seq;
+  for (int j = lane; j < nchunks; j += 32) sm.chunk_blk[qs][j] = __ldg(trow + (tok0 + j * kChunk) / a.block_size);
+  __syncwarp();
+  if (lane == 0) {
+    sm.unit[qs] = make_int4(s, h, it.y, ntok);
+    sm.unit_nparts[qs] = it.w >> 11;
+    sm.unit_tok0[qs] = tok0;
+    __threadfence_block();
+    mbar_arrive_expect_tx(&sm.ufull[qs], D * sizeof(T));
+    bulk_g2s(sm.qbuf[qs], static_cast<const T*>(a.q) + ((size_t)s * H + h) * D, D * sizeof(T), &sm.ufull[qs]);
+  }
+  return true;
+}
+
+// Scheduler and merger (one warp).  Keeps kUnitQueue units published ahead
+// of the consumers; when the consumer warps have all left their share of
+// unit k, merges them (lane i owns output dimensions i, i+32, ...), writes
+// the output or the partition's partial, and refills the slot with unit
+// k + kUnitQueue.  The merge latency (global fences, the cross-partition
+// merge) thus never stalls the warps that stream K and V.
 template <int D, typename T>
 __device__ __forceinline__ void run_scheduler(const DecodeArgs& a, DecodeSmem<D, T>& sm, int lane) {
   volatile int* abort_flag = &sm.abort_flag;
   const int H = a.num_heads;
-  const int P = a.partition_size;
   const long long total_units = (long long)__ldg(a.counters + 1) * H;
-  int issued = 0;
-  for (int k = 0;; ++k) {
+  int published = 0;  // real units published
+  bool more = true;
+  while (more && published < kUnitQueue) {
+    more = publish_unit<D, T>(a, sm, published, total_units, lane);
+    if (more) ++published;
+  }
+  bool aborted = false;
+  for (int k = 0; k < published; ++k) {
     const int qs = k % kUnitQueue;
-    const uint32_t par = (k / kUnitQueue) & 1;
-    int u = 0;
-    if (lane == 0) u = atomicAdd(a.counters, 1);
-    u = __shfl_sync(0xffffffffu, u, 0);
     int ok = 1;
-    if (lane == 0) ok = mbar_wait(&sm.uempty[qs], par ^ 1, abort_flag, a.err_flag);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) break;
-    if ((long long)u >= total_units) {
-      if (lane == 0) {
-        sm.unit[qs] = make_int4(-1, 0, 0, 0);
-        mbar_arrive(&sm.ufull[qs]);
-      }
+    if (lane == 0) ok = mbar_wait(&sm.udone[qs], (k / kUnitQueue) & 1, abort_flag, a.err_flag);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+      aborted = true;
       break;
     }
-    const int item = u / H;
-    const int h = u - item * H;
-    const int2 it = __ldg(a.items + item);
-    const int s = it.x;
-    const int p = it.y;
-    const int ctx = __ldg(a.context_lens + s);
-    const int tok0 = p * P;
-    const int ntok = min(P, ctx - tok0);
-    const int nchunks = (ntok + kChunk - 1) / kChunk;
-    const int32_t* trow = a.block_tables + (size_t)s * a.max_blocks_per_seq;
-    for (int j = lane; j < nchunks; j += 32) sm.chunk_blk[qs][j] = __ldg(trow + (tok0 + j * kChunk) / a.block_size);
     __syncwarp();
-    if (lane == 0) {
-      sm.unit[qs] = make_int4(s, h, p, ntok);
-      sm.unit_nparts[qs] = (ctx + P - 1) / P;
-      __threadfence_block();
-      mbar_arrive_expect_tx(&sm.ufull[qs], D * sizeof(T));
-      bulk_g2s(sm.qbuf[qs], static_cast<const T*>(a.q) + ((size_t)s * H + h) * D, D * sizeof(T), &sm.ufull[qs]);
+    const int4 un = sm.unit[qs];
+    const int nparts = sm.unit_nparts[qs];
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.cm[qs][w]);
+    float L = 0.f;
+    float O[D / 32];
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) O[i] = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = sm.cm[qs][w];
+      const float wt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+      L = fmaf(wt, sm.cl[qs][w], L);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) O[i] = fmaf(wt, sm.co[qs][w][lane + 32 * i], O[i]);
     }
-    ++issued;
+    const int s = un.x, h = un.y, p = un.z;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    if (nparts == 1) {
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i)
+        store_out(a.out, ((size_t)s * H + h) * D + lane + 32 * i, a.out_dtype, O[i] * inv);
+    } else {
+      const size_t pidx = ((size_t)s * H + h) * a.max_parts + p;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) a.part_o[pidx * D + lane + 32 * i] = O[i] * inv;
+      if (lane == 0) a.part_ml[pidx] = make_float2(M, L);
+      __threadfence();
+      __syncwarp();
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(&a.counters[2 + s * H + h], 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == nparts - 1) {  // every partition of (s, h) is in: merge them
+        __threadfence();
+        merge_partitions<D>(a, s, h, nparts, lane);
+      }
+    }
+    __syncwarp();
+    if (more) {
+      more = publish_unit<D, T>(a, sm, k + kUnitQueue, total_units, lane);
+      if (more) ++published;
+    }
   }
-  if (lane == 0 && *abort_flag) {  // let in-flight query copies land before exit
-    for (int kk = max(0, issued - kUnitQueue); kk < issued; ++kk)
+  if (lane == 0 && aborted) {  // let in-flight query copies land before exit
+    for (int kk = max(0, published - kUnitQueue); kk < published; ++kk)
       mbar_wait_drain(&sm.ufull[kk % kUnitQueue], (kk / kUnitQueue) & 1);
   }
 }
@@ -305,10 +398,11 @@ __device__ __forceinline__ void run_producer(const DecodeArgs& a, DecodeSmem<D, 
   volatile int* abort_flag = &sm.abort_flag;
   const int H = a.num_heads;
   const int B = a.block_size;
-  const int P = a.partition_size;
   const T* kp = static_cast<const T*>(a.k_pool);
   const T* vp = static_cast<const T*>(a.v_pool);
-  uint32_t g = 0;
+  uint32_t cnt[kConsumerWarps];  // tiles handed to each consumer warp so far
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) cnt[w] = 0;
   bool aborted = false;
   for (int k = 0; !aborted; ++k) {
     const int qs = k % kUnitQueue;
@@ -316,51 +410,60 @@ __device__ __forceinline__ void run_producer(const DecodeArgs& a, DecodeSmem<D, 
     const int4 un = sm.unit[qs];
     if (un.x < 0) break;
     const int h = un.y;
-    const int tok0 = un.z * P;
+    const int tok0 = sm.unit_tok0[qs];
     const int nchunks = (un.w + kChunk - 1) / kChunk;
-    for (int j = 0; j < nchunks; ++j) {
-      const int slot = g % kStages;
-      if (!mbar_wait(&sm.empty[slot], ((g / kStages) & 1) ^ 1, abort_flag, a.err_flag)) {
-        aborted = true;
-        break;
+    for (int j0 = 0; j0 < nchunks && !aborted; j0 += kConsumerWarps) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const int j = j0 + w;
+        if (j >= nchunks) break;
+        const int slot = w * kSlotsPerWarp + (int)(cnt[w] % kSlotsPerWarp);
+        if (!mbar_wait(&sm.empty[slot], ((cnt[w] / kSlotsPerWarp) & 1) ^ 1, abort_flag, a.err_flag)) {
+          aborted = true;
+          break;
+        }
+        const int32_t blk = sm.chunk_blk[qs][j];
+        if (blk >= 0 && blk < a.num_blocks) {
+          const int off = (tok0 + j * kChunk) % B;
+          const size_t base = (((size_t)blk * H + h) * B + off) * D;
+          sm.slot_ok[slot] = 1;
+          mbar_arrive_expect_tx(&sm.full[slot], 2 * kTileBytes);
+          bulk_g2s(sm.ring[slot][0], kp + base, kTileBytes, &sm.full[slot]);
+          bulk_g2s(sm.ring[slot][1], vp + base, kTileBytes, &sm.full[slot]);
+        } else {
+          sm.slot_ok[slot] = 0;
+          atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
+          mbar_arrive(&sm.full[slot]);
+        }
+        ++cnt[w];
       }
-      const int32_t blk = sm.chunk_blk[qs][j];
-      if (blk >= 0 && blk < a.num_blocks) {
-        const int off = (tok0 + j * kChunk) % B;
-        const size_t base = (((size_t)blk * H + h) * B + off) * D;
-        sm.slot_ok[slot] = 1;
-        mbar_arrive_expect_tx(&sm.full[slot], 2 * kTileBytes);
-        bulk_g2s(sm.ring[slot][0], kp + base, kTileBytes, &sm.full[slot]);
-        bulk_g2s(sm.ring[slot][1], vp + base, kTileBytes, &sm.full[slot]);
-      } else {
-        sm.slot_ok[slot] = 0;
-        atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
-        mbar_arrive(&sm.full[slot]);
-      }
-      ++g;
     }
-    if (!aborted) mbar_arrive(&sm.uempty[qs]);
   }
   if (*abort_flag) {  // let in-flight tile copies land before exit
-    const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0;
-    for (uint32_t gg = first; gg < g; ++gg) mbar_wait_drain(&sm.full[gg % kStages], (gg / kStages) & 1);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const uint32_t first = cnt[w] > (uint32_t)kSlotsPerWarp ? cnt[w] - kSlotsPerWarp : 0;
+      for (uint32_t i = first; i < cnt[w]; ++i)
+        mbar_wait_drain(&sm.full[w * kSlotsPerWarp + i % kSlotsPerWarp], (i / kSlotsPerWarp) & 1);
+    }
   }
 }
 
+// Consumer warp: streams its tiles of each unit (every 4th tile, from its
+// own ring slots, in order), then leaves its (max, sum, output) share of the
+// unit in shared memory for the merger and moves straight on.
 template <int D, typename T>
 __device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, T>& sm, int warp, int lane) {
   constexpr int VPL = D / 64;
   volatile int* abort_flag = &sm.abort_flag;
-  const int H = a.num_heads;
   const int c = lane & 7;
-  uint32_t g = 0;
+  uint32_t mine = 0;  // tiles this warp has taken so far (its own slots, in order)
   for (int k = 0;; ++k) {
     const int qs = k % kUnitQueue;
     bool ok = mbar_wait(&sm.ufull[qs], (k / kUnitQueue) & 1, abort_flag, a.err_flag);
     if (!__all_sync(0xffffffffu, ok)) break;
     const int4 un = sm.unit[qs];
     if (un.x < 0) break;
-    const int nparts = sm.unit_nparts[qs];
     float qf[8 * VPL];
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
@@ -369,8 +472,6 @@ __device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, 
     }
 #pragma unroll
     for (int e = 0; e < 8 * VPL; ++e) qf[e] *= a.qscale;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.uempty[qs]);
 
     const int ntok = un.w;
     const int nchunks = (ntok + kChunk - 1) / kChunk;
@@ -379,10 +480,9 @@ __device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, 
 #pragma unroll
     for (int e = 0; e < 8 * VPL; ++e) o[e] = 0.f;
     bool aborted = false;
-    for (int j = warp; j < nchunks; j += kConsumerWarps) {
-      const uint32_t gg = g + j;
-      const int slot = gg % kStages;
-      ok = mbar_wait(&sm.full[slot], (gg / kStages) & 1, abort_flag, a.err_flag);
+    for (int j = warp; j < nchunks; j += kConsumerWarps, ++mine) {
+      const int slot = warp * kSlotsPerWarp + (int)(mine % kSlotsPerWarp);
+      ok = mbar_wait(&sm.full[slot], (mine / kSlotsPerWarp) & 1, abort_flag, a.err_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         aborted = true;
         break;
@@ -394,9 +494,8 @@ __device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, 
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
     if (aborted) break;
-    g += nchunks;
 
-    // merge the 4 token groups of the warp
+    // merge the 4 token groups of the warp, leave the share for the merger
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
 #pragma unroll
@@ -404,60 +503,23 @@ __device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, 
       o[e] += __shfl_xor_sync(0xffffffffu, o[e], 8);
       o[e] += __shfl_xor_sync(0xffffffffu, o[e], 16);
     }
-    const int cb = k & 1;
     if (lane < 8) {
 #pragma unroll
       for (int v = 0; v < VPL; ++v)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sm.co[cb][warp][(lane + 8 * v) * 8 + e] = o[v * 8 + e];
+        for (int e = 0; e < 8; ++e) sm.co[qs][warp][(lane + 8 * v) * 8 + e] = o[v * 8 + e];
     }
     if (lane == 0) {
-      sm.cm[cb][warp] = m;
-      sm.cl[cb][warp] = l;
+      sm.cm[qs][warp] = m;
+      sm.cl[qs][warp] = l;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.comb[cb]);
-    ok = mbar_wait(&sm.comb[cb], (k >> 1) & 1, abort_flag, a.err_flag);
-    if (!__all_sync(0xffffffffu, ok)) break;
-
-    // merge the consumer warps: thread t owns output dimension t
-    if (warp < D / 32) {
-      const int t = warp * 32 + lane;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.cm[cb][w]);
-      float L = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = sm.cm[cb][w];
-        const float wt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        L = fmaf(wt, sm.cl[cb][w], L);
-        O = fmaf(wt, sm.co[cb][w][t], O);
-      }
-      const int s = un.x, h = un.y, p = un.z;
-      const float val = L > 0.f ? O / L : 0.f;
-      if (nparts == 1) {
-        store_out(a.out, ((size_t)s * H + h) * D + t, a.out_dtype, val);
-      } else {
-        const size_t pidx = ((size_t)s * H + h) * a.max_parts + p;
-        a.part_o[pidx * D + t] = val;
-        if (t == 0) a.part_ml[pidx] = make_float2(M, L);
-        __threadfence();
-        __syncwarp();
-        int prev = 0;
-        if (lane == 0) prev = atomicAdd(&a.counters[2 + s * H + h], 1);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == nparts * (D / 32) - 1) {
-          __threadfence();
-          merge_partitions<D>(a, s, h, nparts, lane);
-        }
-      }
-    }
+    if (lane == 0) mbar_arrive(&sm.udone[qs]);
   }
 }
 
 template <int D, typename T>
-__global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads, PA_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t decode_smem_raw[];
   auto& sm = *reinterpret_cast<DecodeSmem<D, T>*>(decode_smem_raw);
   const int warp = threadIdx.x >> 5;
@@ -469,10 +531,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const DecodeA
     }
     for (int i = 0; i < kUnitQueue; ++i) {
       mbar_init(&sm.ufull[i], 1);
-      mbar_init(&sm.uempty[i], kConsumerWarps + 1);
+      mbar_init(&sm.udone[i], kConsumerWarps);
     }
-    mbar_init(&sm.comb[0], kConsumerWarps);
-    mbar_init(&sm.comb[1], kConsumerWarps);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -505,7 +565,7 @@ WsLayout ws_layout(int S, int H, int D, int max_parts) {
   w.counters = off;
   off = align_up(off + sizeof(int) * (2 + (size_t)S * H), 256);
   w.items = off;
-  off = align_up(off + sizeof(int2) * (size_t)S * max_parts, 256);
+  off = align_up(off + sizeof(int4) * (size_t)S * max_parts, 256);
   w.ml = off;
   off = align_up(off + sizeof(float2) * (size_t)S * H * max_parts, 256);
   w.o = off;
@@ -513,6 +573,9 @@ WsLayout ws_layout(int S, int H, int D, int max_parts) {
   w.total = off;
   return w;
 }
+
+// Partitions of the longest sequence.
+int decode_max_parts(int max_ctx, int P) { return max_ctx > 0 ? (max_ctx + P - 1) / P : 1; }
 
 int resolve_partition(int S, int H, int max_ctx, int partition_size) {
   if (partition_size == 0) return pa_decode_partition_size(S, H, max_ctx);
@@ -581,7 +644,7 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
   if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
   const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
   if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return 0;
-  const int max_parts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
+  const int max_parts = decode_max_parts(max_context_len, P);
   return ws_layout(num_seqs, num_heads, head_dim, max_parts).total;
 }
 
@@ -604,7 +667,7 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
   if ((long long)num_seqs * num_heads > (1ll << 30)) return PA_ERR_INVALID_ARG;
   const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
   if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return PA_ERR_INVALID_ARG;
-  const int max_parts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
+  const int max_parts = decode_max_parts(max_context_len, P);
   const WsLayout w = ws_layout(num_seqs, num_heads, head_dim, max_parts);
   if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
 
@@ -627,7 +690,7 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
   a.max_parts = max_parts;
   char* ws = static_cast<char*>(workspace);
   a.counters = reinterpret_cast<int*>(ws + w.counters);
-  a.items = reinterpret_cast<int2*>(ws + w.items);
+  a.items = reinterpret_cast<int4*>(ws + w.items);
   a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
   a.part_o = reinterpret_cast<float*>(ws + w.o);
   a.err_flag = err_flag;

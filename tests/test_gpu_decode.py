@@ -223,3 +223,24 @@ def test_decode_many_heads_short_contexts(pa):
     out, flags = run_decode(pa, w, out_dtype="f16")
     assert flags == 0
     assert_attn_close(out, oracle_decode(w), "f16", "many heads")
+
+
+def test_decode_many_small_units_stress(pa):
+    """Hundreds of one- and two-tile units per CTA (partition 16 and 32):
+    unit boundaries are everywhere, so consumer warps run ahead of one
+    another constantly.  Repeated launches must give bitwise identical
+    outputs that match the oracle."""
+    g = torch.Generator().manual_seed(11)
+    ctx = tuple(int(x) for x in torch.randint(1, 120, (48,), generator=g))
+    w = W.small_decode(ctx=ctx, H=24, D=128, dtype="f16")
+    ref = oracle_decode(w)
+    dev = torch.device("cuda")
+    kp, vp, q = w.k_pool.to(dev), w.v_pool.to(dev), w.q.to(dev)
+    for P in (16, 32):
+        first, flags = run_decode(pa, w, out_dtype="f32", partition_size=P, kp=kp, vp=vp, q=q)
+        assert flags == 0
+        assert_attn_close(first, ref, "f32", f"stress partition {P}")
+        for _ in range(30):
+            again, flags = run_decode(pa, w, out_dtype="f32", partition_size=P, kp=kp, vp=vp, q=q)
+            assert flags == 0
+            assert torch.equal(first, again)

@@ -150,6 +150,40 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
               int partition_size, int32_t* err_flag, void* stream);
 
 /*
+ * pa_decode_static_scratch -- pa_decode without any device allocation by
+ * anyone.  The paper has no counterpart: this is an interface of this
+ * library only.
+ *
+ * pa_decode needs a few megabytes of device scratch (the work list and the
+ * split-KV partials) that its caller normally allocates.  Some callers cannot
+ * do that: a plugin that is handed only its input and output buffers by a
+ * host framework owning all device memory, or code on a latency-critical path
+ * where cudaMalloc / cudaFree would implicitly synchronise the device.  This
+ * entry point takes the same arguments as pa_decode minus the workspace and
+ * uses instead a fixed array of PA_DECODE_STATIC_SCRATCH_BYTES (16 MiB) that
+ * lives in the library's device code and stays resident on every GPU that
+ * loads the library until the process exits.
+ *  - Limit: if pa_decode_workspace_bytes() for these sizes exceeds
+ *    PA_DECODE_STATIC_SCRATCH_BYTES, it returns PA_ERR_WORKSPACE and launches
+ *    nothing (the LLaMA-13B-shaped batch of 64 sequences x 40 heads with
+ *    contexts up to 2048 needs about 5.3 MiB; 256 x 32 heads with contexts up
+ *    to 16384 does not fit and must use pa_decode).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.  Nothing is allocated, then or later.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind; no initial contents are needed (each call's planning kernel
+ *    resets the counters it uses).  Calls that can overlap on the GPU (other
+ *    streams, other threads) race on the array: serialise them.
+ */
+#define PA_DECODE_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int pa_decode_static_scratch(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
+                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                             int max_context_len, int num_seqs, int num_heads, int head_dim, int block_size,
+                             int num_blocks, float scale, int dtype, int partition_size, int32_t* err_flag,
+                             void* stream);
+
+/*
  * pa_prefill_chunk -- causal attention of prefill chunks over paged K/V.
  * [cb] "Chunked prefill": a long prompt is split into chunks processed over
  * several steps; [summary] section 4 equation, causal j <= i.

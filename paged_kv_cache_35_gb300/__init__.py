@@ -51,6 +51,7 @@ SIGNATURES = {
     "pa_decode_partition_size": ([_I, _I, _I], _I),
     "pa_decode_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
     "pa_decode": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _I, _P, _P], _I),
+    "pa_decode_static_scratch": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P], _I),
     "pa_prefill_chunk": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P], _I),
     "pa_get_error": ([_P, _P, _P], _I),
     "pa_slot_mapping": ([_P, _I, _I, _I, _P, _P, _I, _P], _I),
@@ -196,6 +197,25 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, max_context_le
         _kv_code(k_pool), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         int(partition_size), _dev(err_flag, "err_flag", torch.int32), _stream(stream))
     _check(st, "pa_decode")
+
+
+def pa_decode_static_scratch(out, q, k_pool, v_pool, block_tables, context_lens, max_context_len, scale, err_flag,
+                             partition_size=0, stream=None):
+    """pa_decode with the library's fixed device scratch instead of a caller
+    workspace, for callers that cannot allocate device memory (see pa.h)."""
+    NB, H, B, D = k_pool.shape
+    S = q.shape[0]
+    if tuple(q.shape) != (S, H, D) or tuple(out.shape) != (S, H, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] < S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [>=S][MB], context_lens [S]")
+    st = lib().pa_decode_static_scratch(
+        _dev(out, "out", (torch.float16, torch.bfloat16, torch.float32)), _TORCH_TO_PA[out.dtype],
+        _dev(q, "q", k_pool.dtype), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, D, B, NB, float(scale),
+        _kv_code(k_pool), int(partition_size), _dev(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "pa_decode_static_scratch")
 
 
 def pa_prefill_chunk(out, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables, max_q_len, scale, err_flag,

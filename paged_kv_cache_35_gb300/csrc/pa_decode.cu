@@ -44,6 +44,8 @@
 //  * Every wait is bounded; bad table entries are flagged, never trapped.
 #include <math.h>
 
+#include <mutex>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -702,3 +704,38 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// pa_decode_static_scratch: pa_decode for callers that cannot allocate device
+// memory.  Its scratch is this fixed array, resident on every device that
+// loads the library; the host looks its address up once per device.
+static __device__ __align__(256) unsigned char g_decode_static_scratch[PA_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_static_scratch_mutex;
+void* g_static_scratch_addr[64] = {nullptr};
+}  // namespace
+
+extern "C" int pa_decode_static_scratch(void* out, int out_dtype, const void* q, const void* k_pool,
+                                        const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                                        const int32_t* context_lens, int max_context_len, int num_seqs,
+                                        int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                                        int dtype, int partition_size, int32_t* err_flag, void* stream) {
+  const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size);
+  if (need > (size_t)PA_DECODE_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+    if (g_static_scratch_addr[dev] == nullptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_decode_static_scratch) != cudaSuccess || addr == nullptr) return PA_ERR_CUDA;
+      g_static_scratch_addr[dev] = addr;
+    }
+    scratch = g_static_scratch_addr[dev];
+  }
+  return pa_decode(out, out_dtype, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                   max_context_len, num_seqs, num_heads, head_dim, block_size, num_blocks, scale, dtype, scratch,
+                   (size_t)PA_DECODE_STATIC_SCRATCH_BYTES, partition_size, err_flag, stream);
+}

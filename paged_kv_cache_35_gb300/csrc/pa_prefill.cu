@@ -64,6 +64,8 @@ constexpr uint32_t kOffK = kOffQ + kTileBytes;       // 2 stages
 constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;   // 2 stages
 constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;   // P_hi, then P_lo
 constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kPfRankMax = 1024;  // (chunk, query tile) pairs ranked in-kernel
+
 struct PfBars {
   uint64_t q_full;
   uint64_t kv_full[2], kv_empty[2];
@@ -88,6 +90,9 @@ struct PrefillArgs {
   int block_size;
   int num_blocks;
   int rows_per_load;  // min(block_size, 128)
+  int rpl_shift;      // log2(rows_per_load)
+  int num_chunks;
+  int qtiles;         // query tiles per chunk in the grid: ceil(max_q_len / 128)
   float qscale;       // scale * log2(e)
   uint32_t idesc_s;   // instruction descriptors
   uint32_t idesc_pv;
@@ -157,6 +162,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 128 consecutive fp32 columns of this thread's TMEM lane, load and wait in
+// one asm statement.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* v) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2^x by the hardware's approximate base-2 exponential (relative error
+// below 2^-22; 2^-inf = +0), flushing subnormal results to zero.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -189,16 +216,25 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// x rounded (to nearest even) to the 16-bit type T, returned as float.
+// (x, y) as two packed 16-bit pairs: hi = (x, y) rounded to T, lo = the
+// remainders rounded to T, so that hi + lo carries ~16 significant bits.
 template <typename T>
-__device__ __forceinline__ float round_to(float x);
+__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo);
 template <>
-__device__ __forceinline__ float round_to<__half>(float x) {
-  return __half2float(__float2half_rn(x));
+__device__ __forceinline__ void split2<__half>(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x, y);
+  const float2 hf = __half22float2(h);
+  const __half2 r = __floats2half2_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 template <>
-__device__ __forceinline__ float round_to<__nv_bfloat16>(float x) {
-  return __bfloat162float(__float2bfloat16_rn(x));
+__device__ __forceinline__ void split2<__nv_bfloat16>(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
@@ -219,11 +255,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // later tiles (more keys) start first
-  const int h = blockIdx.y;
-  const int c = blockIdx.z;
   const int H = a.num_heads;
   const int B = a.block_size;
+  // Work order: the grid is 1-D over (chunk, query tile) pairs x heads.  The
+  // pairs are taken longest first (most key tiles), so the hardware's
+  // in-order dispatch schedules the long CTAs before the short ones.  Every
+  // CTA ranks the pairs itself from the chunk lengths (when there are at most
+  // kPfRankMax pairs; otherwise pairs go in their natural order).
+  const int npairs = a.num_chunks * a.qtiles;
+  const int my_rank = blockIdx.x / H;
+  const int h = blockIdx.x - my_rank * H;
+  int pair = my_rank;
+  if (npairs <= kPfRankMax) {
+    int* cost = reinterpret_cast<int*>(gbase + kOffP);  // scratch, before the P buffers are used
+    int* chosen = cost + kPfRankMax;
+    for (int e = threadIdx.x; e < npairs; e += blockDim.x) {
+      const int cc = e / a.qtiles, tt = e - cc * a.qtiles;
+      const int nq = __ldg(a.cu_q_lens + cc + 1) - __ldg(a.cu_q_lens + cc);
+      const int last = min(tt * kPfRows + kPfRows - 1, nq - 1);
+      cost[e] = tt * kPfRows < nq ? (__ldg(a.ctx_before + cc) + last) / kPfKeys + 1 : 0;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < npairs; e += blockDim.x) {
+      const int ke = cost[e];
+      int rank = 0;
+      for (int f = 0; f < npairs; ++f) rank += (cost[f] > ke) || (cost[f] == ke && f < e);
+      if (rank == my_rank) chosen[0] = e;
+    }
+    __syncthreads();
+    pair = chosen[0];
+    __syncthreads();
+  }
+  const int c = pair / a.qtiles;
+  const int qt = pair - c * a.qtiles;
 
   const int q0 = __ldg(a.cu_q_lens + c);
   const int n_c = __ldg(a.cu_q_lens + c + 1) - q0;
@@ -370,7 +434,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int qrow = qt * kPfRows + row;
     const int pos = c0 + qrow;
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    const int rpl = a.rows_per_load;
+    const uint32_t full_mask = (1u << (kPfKeys / a.rows_per_load)) - 1u;
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -385,33 +449,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       tc_fence_after();
       float s[kPfKeys];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(lane_addr + (st ? kTmemS1 : kTmemS0) + cc * 32, s + cc * 32);
+      tmem_ld128(lane_addr + (st ? kTmemS1 : kTmemS0), s);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.s_empty[st]);
 
       const int key0 = j * kPfKeys;
       const uint32_t kmask = bars.kv_mask[st];
-      const int lim = min(pos, ctx_total - 1) - key0;  // last admissible column
-      float rmax = -INFINITY;
+      // interior tile: every key precedes every query of the tile, lies in the
+      // context and was loaded -- no masking at all
+      const bool interior = key0 + kPfKeys - 1 <= c0 + qt * kPfRows && key0 + kPfKeys <= ctx_total &&
+                            kmask == full_mask;
+      if (!interior) {
+        const int lim = min(pos, ctx_total - 1) - key0;  // last admissible column of this row
 #pragma unroll
-      for (int col = 0; col < kPfKeys; ++col) {
-        const bool valid = col <= lim && ((kmask >> (col / rpl)) & 1u);
-        s[col] = valid ? s[col] * a.qscale : -INFINITY;
-        rmax = fmaxf(rmax, s[col]);
+        for (int col = 0; col < kPfKeys; ++col) {
+          const bool valid = col <= lim && ((kmask >> (col >> a.rpl_shift)) & 1u);
+          s[col] = valid ? s[col] : -INFINITY;
+        }
       }
+      float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+      for (int col = 4; col < kPfKeys; ++col) mx4[col & 3] = fmaxf(mx4[col & 3], s[col]);
+      const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.qscale;  // qscale > 0
       const float m_new = fmaxf(m_used, rmax);
       const bool resc = m_new > m_used + kRescaleThreshold;  // also true when m_used is -inf
       const float m_next = resc ? m_new : m_used;
-      const float alpha = resc ? ((m_used == -INFINITY) ? 0.f : exp2f(m_used - m_next)) : 1.f;
+      const float alpha = resc ? ((m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_next)) : 1.f;
       l *= alpha;
       const float mref = (m_next == -INFINITY) ? 0.f : m_next;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int col = 0; col < kPfKeys; ++col) {
-        s[col] = exp2f(s[col] - mref);
-        l += s[col];
+        s[col] = ex2_approx(fmaf(s[col], a.qscale, -mref));
+        sum4[col & 3] += s[col];
       }
+      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // P_{j-1} V_{j-1} must be complete: it reads the P buffer written below
       // and it is the last product O holds before a rescale
       if (j > 0) {
@@ -421,17 +494,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            tmem_ld32(lane_addr + kTmemO + cc * 32, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_addr + kTmemO + cc * 32, o);
-          }
-          tmem_st_wait();
-        }
       }
       uint8_t* phi = gbase + kOffP;
       uint8_t* plo = gbase + kOffP + kTileBytes;
@@ -440,29 +502,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const float* src = s + half * 64 + ch * 8;
-          float hi[8], lo[8];
+          uint32_t hw[4], lw[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            hi[e] = round_to<T>(src[e]);
-            lo[e] = src[e] - hi[e];
-          }
-          uint4 vh, vl;
-          vh.x = pack2<T>(hi[0], hi[1]);
-          vh.y = pack2<T>(hi[2], hi[3]);
-          vh.z = pack2<T>(hi[4], hi[5]);
-          vh.w = pack2<T>(hi[6], hi[7]);
-          vl.x = pack2<T>(lo[0], lo[1]);
-          vl.y = pack2<T>(lo[2], lo[3]);
-          vl.z = pack2<T>(lo[4], lo[5]);
-          vl.w = pack2<T>(lo[6], lo[7]);
+          for (int e = 0; e < 4; ++e) split2<T>(src[2 * e], src[2 * e + 1], hw[e], lw[e]);
           const uint32_t off = half * kHalfBytes + sw128_offset(row, ch);
-          *reinterpret_cast<uint4*>(phi + off) = vh;
-          *reinterpret_cast<uint4*>(plo + off) = vl;
+          *reinterpret_cast<uint4*>(phi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(plo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
       // key row `row` of V: zero it if it was not loaded or lies past the context
       const int key = key0 + row;
-      if (key >= ctx_total || !((kmask >> (row / rpl)) & 1u)) {
+      if (key >= ctx_total || !((kmask >> (row >> a.rpl_shift)) & 1u)) {
         uint8_t* vbuf = gbase + kOffV + st * kTileBytes;
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -470,6 +520,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           *reinterpret_cast<uint4*>(vbuf + row * 128 + ch * 16) = z;
           *reinterpret_cast<uint4*>(vbuf + kHalfBytes + row * 128 + ch * 16) = z;
         }
+      }
+      // rescale O in tensor memory when the running max moved (after P is
+      // stored, so the probabilities are no longer held in registers)
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(lane_addr + kTmemO + cc * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(lane_addr + kTmemO + cc * 32, o);
+        }
+        tmem_st_wait();
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -574,7 +637,7 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
   if (num_chunks < 0 || total_q < 0 || max_q_len < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
     return PA_ERR_INVALID_ARG;
   if (num_chunks == 0 || total_q == 0 || max_q_len == 0) return PA_OK;
-  if (num_chunks > 65535 || num_heads > 65535) return PA_ERR_INVALID_ARG;
+  if (num_heads > 65535) return PA_ERR_INVALID_ARG;
   if (!out || !q || !cu_q_lens || !ctx_before || !k_pool || !v_pool || !block_tables || !err_flag)
     return PA_ERR_INVALID_ARG;
   if (!pa_host::aligned16(q) || !pa_host::aligned16(k_pool) || !pa_host::aligned16(v_pool) ||
@@ -621,6 +684,7 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
   a.block_size = block_size;
   a.num_blocks = num_blocks;
   a.rows_per_load = rows_per_load;
+  a.rpl_shift = 31 - __builtin_clz((unsigned)rows_per_load);
   a.qscale = scale * 1.4426950408889634f;
   const uint32_t fmt = dtype == PA_BF16 ? 1u : 0u;
   a.idesc_s = make_idesc(fmt, false);
@@ -637,7 +701,11 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
       return PA_ERR_CUDA;
     configured[fmt][dev] = 1;
   }
-  dim3 grid((max_q_len + pa::kPfRows - 1) / pa::kPfRows, num_heads, num_chunks);
+  a.num_chunks = num_chunks;
+  a.qtiles = (max_q_len + pa::kPfRows - 1) / pa::kPfRows;
+  const long long nblocks = (long long)a.qtiles * num_chunks * num_heads;
+  if (nblocks >= (1ll << 31)) return PA_ERR_INVALID_ARG;
+  dim3 grid((unsigned)nblocks);
   kern<<<grid, pa::kPfThreads, pa::kPfSmemBytes, (cudaStream_t)stream>>>(tm_q, tm_k, tm_v, a);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -183,25 +183,43 @@ def workload_config(w, NB):
             "l2": "no flush: K/V read per step (~1.4 GB) >> 129 MB L2"}
 
 
-def cpu_oracle_time(w, host, budget_s: float, max_reps: int = 1000):
-    """Time the oracle (scatter + decode) on the whole workload, repeated
-    until ~budget_s.  Returns (seconds per rep, reps, threads)."""
-    import numpy as np
+class OracleStep:
+    """The CPU oracle's version of one step (slot scatter + decode) on a
+    workload, with the inputs converted to bit arrays once, outside any
+    timing.  `rows` restricts the step to a subset of the sequences."""
 
-    import oracle
+    def __init__(self, w, host, rows=None):
+        import numpy as np
 
-    kb0, vb0 = oracle.pool_bits(host["k_pool"]), oracle.pool_bits(host["v_pool"])
-    tb = w.block_tables.numpy()
-    slots = np.array([oracle.slot_of(tb[s], int(w.new_pos[s]), w.block_size) for s in range(w.num_seqs)],
-                     dtype=np.int64)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.reshape_and_cache(host["k_new"], host["v_new"], kb0, vb0, slots, w.block_size)
-        oracle.decode(host["q"], kb0, vb0, w.block_tables, w.context_lens, w.block_size, w.scale, "f16")
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or reps >= max_reps:
-            return el / reps, reps, oracle.num_threads()
+        import oracle
+
+        self.oracle = oracle
+        self.w = w
+        rows = list(range(w.num_seqs)) if rows is None else list(rows)
+        self.kb, self.vb = oracle.pool_bits(host["k_pool"]), oracle.pool_bits(host["v_pool"])
+        tb = w.block_tables.numpy()
+        self.tables = np.ascontiguousarray(tb[rows])
+        self.ctx = np.ascontiguousarray(w.context_lens.numpy()[rows])
+        self.slots = np.array([oracle.slot_of(tb[s], int(w.new_pos[s]), w.block_size) for s in rows], dtype=np.int64)
+        self.q = host["q"][rows].contiguous()
+        self.k_new = host["k_new"][rows].contiguous()
+        self.v_new = host["v_new"][rows].contiguous()
+        self.rows = rows
+
+    def run(self):
+        o, w = self.oracle, self.w
+        o.reshape_and_cache(self.k_new, self.v_new, self.kb, self.vb, self.slots, w.block_size)
+        return o.decode(self.q, self.kb, self.vb, self.tables, self.ctx, w.block_size, w.scale, w.dtype)
+
+    def time(self, budget_s: float, max_reps: int = 1000):
+        """Repeat run() until ~budget_s; returns (seconds per run, runs)."""
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            self.run()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or reps >= max_reps:
+                return el / reps, reps
 
 
 def run_reference(args, rank, world):
@@ -219,25 +237,22 @@ def run_reference(args, rank, world):
     elt = 2
     step_b = decode_bytes(w.context_lens.tolist(), w.num_heads, w.head_dim, w.block_size, elt) + scatter_bytes(
         w.num_seqs, w.num_heads, w.head_dim, elt)
-    # warm-up reps (untimed), then K timed steps; each step is the whole
+    # warm-up steps (untimed), then K timed steps; each step is the whole
     # workload unless that would exceed ~60 s in total, in which case each
     # step runs on a fixed subset of the sequences.
-    t_one, _, thr = cpu_oracle_time(w, host, 0.0, 1)
-    for _ in range(max(0, args.warmup - 1)):
-        cpu_oracle_time(w, host, 0.0, 1)
+    full = OracleStep(w, host)
+    thr = oracle.num_threads()
+    t_one, _ = full.time(0.0, 1)
     frac = min(1.0, 60.0 / max(1e-9, t_one * args.steps))
     nsub = max(1, int(w.num_seqs * frac))
-    sub = W.DecodeWorkload(**{**w.__dict__})
-    idx = torch.arange(nsub)
-    sub.context_lens, sub.new_pos = w.context_lens[idx], w.new_pos[idx]
-    sub.block_tables = w.block_tables[idx]
-    sub_host = {"k_pool": host["k_pool"], "v_pool": host["v_pool"], "q": host["q"][idx], "k_new": host["k_new"][idx],
-                "v_new": host["v_new"][idx]}
-    sub_b = decode_bytes(sub.context_lens.tolist(), w.num_heads, w.head_dim, w.block_size, elt) + scatter_bytes(
+    step = full if nsub == w.num_seqs else OracleStep(w, host, rows=range(nsub))
+    for _ in range(max(0, args.warmup - 1)):
+        step.run()
+    sub_b = decode_bytes(step.ctx.tolist(), w.num_heads, w.head_dim, w.block_size, elt) + scatter_bytes(
         nsub, w.num_heads, w.head_dim, elt)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        cpu_oracle_time(sub, sub_host, 0.0, 1)
+        step.run()
     el = time.perf_counter() - t0
     gbs = sub_b * args.steps / el / 1e9
     sample = (f"{nsub} of {w.num_seqs} sequences x {w.num_heads} heads per step" if nsub < w.num_seqs
@@ -384,9 +399,11 @@ def run_ours(args, rank, world, local):
         "clocks": clocks.summary(h0, h1),
     }
     if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+
         host = {k: getattr(w, k).cpu() for k in ("k_pool", "v_pool", "q", "k_new", "v_new")}
-        wc = W.DecodeWorkload(**{**w.__dict__})
-        t_rep, reps, thr = cpu_oracle_time(wc, host, args.cpu_budget)
+        t_rep, reps = OracleStep(w, host).time(args.cpu_budget)
+        thr = oracle.num_threads()
         line["cpu_baseline"] = {"value": step_b / t_rep / 1e9, "unit": "GB/s", "cores": thr, "kind": "oracle",
                                 "sample": f"whole workload (scatter + decode), {reps} repetitions, "
                                           f"{t_rep * reps:.1f} s wall"}

@@ -56,6 +56,16 @@ def kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def load_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured bf16 dense (burst)"
+    except Exception:
+        return 1900.0, "fallback bf16 dense"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -173,14 +183,77 @@ def dist_barrier(world: int):
         dist.barrier()
 
 
-# ---- workload ---------------------------------------------------------------------------------------
-def workload_config(w, NB):
-    return {"workload": "llama13b_decode_b64: 64 seqs x 40 heads x 128, block 16, ctx U[128,2048], fp16",
-            "num_seqs": w.num_seqs, "num_heads": w.num_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-            "pool_blocks": NB, "context_lens": "uniform [128, 2048], seed 1", "kv_dtype": "fp16",
-            "placement": "seeded random permutation of the pool",
-            "step": "pa_reshape_and_cache (1 new token/seq) + pa_decode over ctx",
-            "l2": "no flush: K/V read per step (~1.4 GB) >> 129 MB L2"}
+# ---- workloads ----------------------------------------------------------------------------------------
+WORKLOAD_TEXT = {
+    "llama13b": "llama13b_decode_b64: 64 seqs x 40 heads x 128, block 16, ctx U[128,2048], fp16",
+    "long_context": "long_context_decode_b256: 256 seqs x 32 heads x 128, block 16, ctx log-normal "
+                    "(median 1024, sigma 1, clipped 16..16384), bf16",
+    "tiny": "tiny_paged_decode: 4 seqs x 4 heads x 64, block 16, ctx {1,16,17,45}, 32-block pool, fp16",
+    "shared_prefix": "parallel_sampling_shared_prefix: 8 prompts x 8 samples, prompt 1000, suffix U[1,256], "
+                     "40 heads x 128, block 16, fp16, copy-on-write through the host allocator",
+    "mixed": "mixed_chunked_prefill: 32 decode seqs (ctx U[256,4096]) + 2 chunks x 512 queries at ctx 1024/3072, "
+             "40 heads x 128, page 256, bf16",
+}
+
+
+def workload_config(name, w):
+    return {"workload": WORKLOAD_TEXT[name], "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "pool_blocks": w.num_blocks, "kv_dtype": w.dtype,
+            "placement": "seeded random permutation of the pool" if name != "shared_prefix" else
+            "host allocator (free list from the end, copy-on-write)",
+            "step": "pa_reshape_and_cache (1 new token/seq) + pa_decode over ctx" +
+                    (" + pa_prefill_chunk (2 x 512 queries, their K/V in the same scatter)" if name == "mixed" else ""),
+            "l2": "no flush: K/V read per step >> 129 MB L2" if name in ("llama13b", "long_context", "mixed") else
+                  "working set partly L2-resident (reported as such)"}
+
+
+def shared_prefix_decode_workload(pa, W, dev):
+    """The parallel-sampling state built through the library: prompts written,
+    forked 8 ways, first suffix token of each sample copy-on-writes the
+    shared partial block, suffixes written.  Returned as a decode workload
+    whose step rewrites each sample's newest token and attends over it."""
+    import numpy as np
+    import torch
+
+    sc = W.shared_prefix(device=dev)
+    P, N, L, B, H, D = sc.num_prompts, sc.samples, sc.prompt_len, sc.block_size, sc.num_heads, sc.head_dim
+    n = P * N
+    alloc = pa.BlockAllocator(sc.num_blocks, B)
+    for p in range(P):
+        alloc.add_seq(p * N)
+    pslots = np.stack([alloc.append_slots([p * N for p in range(P)])[0] for _ in range(L)], axis=1)
+    for p in range(P):
+        for j in range(1, N):
+            alloc.fork(p * N, p * N + j)
+    kp, vp = sc.pool_init_k, sc.pool_init_v
+    err = pa.new_error_flag(dev)
+    pa.pa_reshape_and_cache(sc.prompt_k.reshape(P * L, H, D), sc.prompt_v.reshape(P * L, H, D), kp, vp,
+                            torch.from_numpy(pslots.reshape(-1)).to(dev), err)
+    suffix = sc.suffix_lens.tolist()
+    ms = sc.suffix_k.shape[1]
+    sslots = np.full((n, ms), -1, dtype=np.int64)
+    for r in range(max(suffix)):
+        active = [s for s in range(n) if suffix[s] > r]
+        slots, pairs = alloc.append_slots(active)
+        sslots[active, r] = slots
+        if len(pairs):
+            pa.pa_copy_blocks(kp, vp, torch.from_numpy(pairs).to(dev), err)
+    pa.pa_reshape_and_cache(sc.suffix_k.reshape(n * ms, H, D), sc.suffix_v.reshape(n * ms, H, D), kp, vp,
+                            torch.from_numpy(sslots.reshape(-1)).to(dev), err)
+    if pa.pa_get_error(err):
+        raise RuntimeError("device error while building the shared-prefix state")
+    mb = max(len(alloc.block_table(s)[0]) for s in range(n))
+    tables, lens = alloc.block_tables(range(n), mb)
+    lens_t = torch.from_numpy(lens)
+    unique_blocks = sc.num_blocks - alloc.num_free()
+    w = W.DecodeWorkload(
+        name="shared_prefix", num_heads=H, head_dim=D, block_size=B, num_blocks=sc.num_blocks, dtype="f16",
+        context_lens=lens_t, new_pos=(lens_t - 1).to(torch.int32), block_tables=torch.from_numpy(tables),
+        max_blocks_per_seq=mb, q=sc.q, k_new=W.normal((n, H, D), 31, torch.float16, dev),
+        v_new=W.normal((n, H, D), 32, torch.float16, dev), k_pool=kp, v_pool=vp, scale=sc.scale,
+        extra={"unique_kv_bytes": 2 * unique_blocks * H * B * D * 2})
+    alloc.close()
+    return w
 
 
 class OracleStep:
@@ -261,7 +334,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, w.num_blocks),
+        "config": workload_config("llama13b", w),
         "seq_steps_per_s": nsub * args.steps / el,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": sample},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -282,22 +355,53 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = W.llama13b_decode(device=dev)
+    name = args.workload
+    mixed = None
+    if name == "llama13b":
+        w = W.llama13b_decode(device=dev)
+    elif name == "long_context":
+        w = W.long_context_decode(device=dev)
+    elif name == "tiny":
+        w = W.tiny_decode(device=dev)
+    elif name == "shared_prefix":
+        w = shared_prefix_decode_workload(pa, W, dev)
+    else:
+        mixed = W.mixed_prefill(device=dev)
+        w = mixed.decode
     S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
     elt = 2
+    tdt = torch.float16 if w.dtype == "f16" else torch.bfloat16
     slots = pa.pa_slot_mapping(w.block_tables, np.arange(S), w.new_pos, B)
+    k_new, v_new = w.k_new, w.v_new
+    if mixed is not None:  # one scatter: the decode tokens and the chunks' tokens
+        seq_idx = np.concatenate([np.full(int(n), c) for c, n in enumerate(mixed.chunk_lens.tolist())])
+        pos = np.concatenate([np.arange(c0, c0 + n) for c0, n in
+                              zip(mixed.ctx_before.tolist(), mixed.chunk_lens.tolist())])
+        slots = np.concatenate([slots, pa.pa_slot_mapping(mixed.chunk_tables, seq_idx, pos, B)])
+        k_new = torch.cat([w.k_new, mixed.chunk_k])
+        v_new = torch.cat([w.v_new, mixed.chunk_v])
+        T = int(mixed.chunk_lens.sum())
+        pout = torch.empty(T, H, D, dtype=tdt, device=dev)
+        cu_d = torch.cat([torch.zeros(1, dtype=torch.int32), mixed.chunk_lens.cumsum(0).to(torch.int32)]).to(dev)
+        cb_d, ctab_d = mixed.ctx_before.to(dev), mixed.chunk_tables.to(dev)
+        mq = int(mixed.chunk_lens.max())
     slots_d = torch.from_numpy(slots).to(dev)
     tables_d = w.block_tables.to(dev)
     ctx_d = w.context_lens.to(dev)
     mx = int(w.context_lens.max())
-    out = torch.empty(S, H, D, dtype=torch.float16, device=dev)
+    out = torch.empty(S, H, D, dtype=tdt, device=dev)
     ws = pa.decode_workspace(S, H, D, mx, device=dev)
     err = pa.new_error_flag(dev)
     stream = torch.cuda.current_stream(dev)
 
+    def prefill():
+        pa.pa_prefill_chunk(pout, mixed.chunk_q, cu_d, cb_d, w.k_pool, w.v_pool, ctab_d, mq, w.scale, err, stream)
+
     def step():
-        pa.pa_reshape_and_cache(w.k_new, w.v_new, w.k_pool, w.v_pool, slots_d, err, stream)
+        pa.pa_reshape_and_cache(k_new, v_new, w.k_pool, w.v_pool, slots_d, err, stream)
         pa.pa_decode(out, w.q, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err, stream=stream)
+        if mixed is not None:
+            prefill()
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -307,15 +411,21 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device error flags {flags} during warm-up")
 
     dbytes = decode_bytes(w.context_lens.tolist(), H, D, B, elt)
-    sbytes = scatter_bytes(S, H, D, elt)
-    step_b = dbytes + sbytes
+    sbytes = scatter_bytes(k_new.shape[0], H, D, elt)
+    pflops = pbytes = 0
+    if mixed is not None:
+        pflops = sum(4 * D * H * sum(c0 + i + 1 for i in range(n))
+                     for c0, n in zip(mixed.ctx_before.tolist(), mixed.chunk_lens.tolist()))
+        pbytes = sum(2 * (c0 + n) * H * D * elt + 2 * n * H * D * elt
+                     for c0, n in zip(mixed.ctx_before.tolist(), mixed.chunk_lens.tolist()))
+    step_b = dbytes + sbytes + pbytes
 
     # ---- device-timed region
     K = args.steps
-    dec_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    dec_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    dec_s, dec_e = [ev() for _ in range(K)], [ev() for _ in range(K)]
+    pre_s, pre_e = ([ev() for _ in range(K)], [ev() for _ in range(K)]) if mixed is not None else ([], [])
+    t_start, t_end = ev(), ev()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -324,10 +434,14 @@ def run_ours(args, rank, world, local):
     h0 = time.time()
     t_start.record(stream)
     for i in range(K):
-        pa.pa_reshape_and_cache(w.k_new, w.v_new, w.k_pool, w.v_pool, slots_d, err, stream)
+        pa.pa_reshape_and_cache(k_new, v_new, w.k_pool, w.v_pool, slots_d, err, stream)
         dec_s[i].record(stream)
         pa.pa_decode(out, w.q, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err, stream=stream)
         dec_e[i].record(stream)
+        if mixed is not None:
+            pre_s[i].record(stream)
+            prefill()
+            pre_e[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     h1 = time.time()
@@ -335,6 +449,7 @@ def run_ours(args, rank, world, local):
     clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(b) for a, b in zip(dec_s, dec_e)]
+    pre_ms = [a.elapsed_time(b) for a, b in zip(pre_s, pre_e)]
     flags = pa.pa_get_error(err, stream)
     if flags:
         raise RuntimeError(f"device error flags {flags} in the timed region")
@@ -346,27 +461,36 @@ def run_ours(args, rank, world, local):
     # ---- end to end through the API: pinned host inputs in, result out, every step
     Ke = min(K, 200)
     pin = lambda t: t.detach().cpu().pin_memory()
-    h_q, h_k, h_v = pin(w.q), pin(w.k_new), pin(w.v_new)
+    h_q, h_k, h_v = pin(w.q), pin(k_new), pin(v_new)
     h_slots, h_tables, h_ctx = pin(torch.from_numpy(slots)), pin(w.block_tables), pin(w.context_lens)
-    h_out = torch.empty(S, H, D, dtype=torch.float16).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(w.q), torch.empty_like(w.k_new), torch.empty_like(w.v_new)
+    h_out = torch.empty(S, H, D, dtype=tdt).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(w.q), torch.empty_like(k_new), torch.empty_like(v_new)
     d_slots, d_tables, d_ctx = torch.empty_like(slots_d), torch.empty_like(tables_d), torch.empty_like(ctx_d)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tables, h_ctx))
-    d2h = h_out.numel() * h_out.element_size()
+    pairs = [(d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_tables, h_tables), (d_ctx, h_ctx)]
+    outs = [(h_out, out)]
+    if mixed is not None:
+        h_cq, h_pout = pin(mixed.chunk_q), torch.empty(T, H, D, dtype=tdt).pin_memory()
+        d_cq = torch.empty_like(mixed.chunk_q)
+        pairs.append((d_cq, h_cq))
+        outs.append((h_pout, pout))
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
 
     def e2e_step():
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_tables, h_tables), (d_ctx, h_ctx)):
+        for d, h in pairs:
             d.copy_(h, non_blocking=True)
         pa.pa_reshape_and_cache(d_k, d_v, w.k_pool, w.v_pool, d_slots, err, stream)
         pa.pa_decode(out, d_q, w.k_pool, w.v_pool, d_tables, d_ctx, mx, w.scale, ws, err, stream=stream)
-        h_out.copy_(out, non_blocking=True)
+        if mixed is not None:
+            pa.pa_prefill_chunk(pout, d_cq, cu_d, cb_d, w.k_pool, w.v_pool, ctab_d, mq, w.scale, err, stream)
+        for h, d in outs:
+            h.copy_(d, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize(dev)
     dist_barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    e0, e1 = ev(), ev()
     e0.record(stream)
     for _ in range(Ke):
         e2e_step()
@@ -379,12 +503,14 @@ def run_ours(args, rank, world, local):
     dec_avg_s = statistics.mean(dec_ms) / 1e3
     achieved = dbytes / dec_avg_s / 1e9
     sha = kernel_sha()
-    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha256_prefix"] == sha else None
-
+    traffic = (TRAFFIC["bytes_per_launch"] if name == "llama13b" and TRAFFIC["kernel_sha256_prefix"] == sha
+               else None)
+    launches = 3 + (1 if mixed is not None else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic", "config": {**workload_config(w, w.num_blocks), "parallelism": f"replicas x{world}"},
+        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {**workload_config(name, w), "parallelism": f"replicas x{world}"},
         "seq_steps_per_s": seq_steps,
         "hbm_frac_of_measured_peak": value / world / peak,
         "hbm_frac_of_nominal_8tbs": value / world / 8000.0,
@@ -395,17 +521,30 @@ def run_ours(args, rank, world, local):
                      "kernel_sha256_prefix": sha},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / Ke, "steps": Ke},
-        "gpu_launches": 3 * K,
+        "gpu_launches": launches * K,
         "clocks": clocks.summary(h0, h1),
     }
+    if "unique_kv_bytes" in w.extra:
+        line["config"]["unique_kv_bytes"] = w.extra["unique_kv_bytes"]
+        line["roofline"]["note"] = ("logical bytes: shared prompt blocks are counted once per sample that reads "
+                                    "them; the unique K/V footprint is config.unique_kv_bytes")
+    if mixed is not None:
+        bf16_peak = load_tensor_peak()
+        pre_avg_s = statistics.mean(pre_ms) / 1e3
+        line["prefill"] = {"bound": "tensor", "achieved": pflops / pre_avg_s / 1e12, "unit": "TFLOP/s",
+                           "peak": bf16_peak[0], "frac": pflops / pre_avg_s / 1e12 / bf16_peak[0],
+                           "peak_kind": bf16_peak[1], "algorithmic_flops_per_launch": pflops,
+                           "avg_launch_ms": pre_avg_s * 1e3,
+                           "tensor_flops_executed_per_launch": pflops * 3 // 2}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
 
         host = {k: getattr(w, k).cpu() for k in ("k_pool", "v_pool", "q", "k_new", "v_new")}
         t_rep, reps = OracleStep(w, host).time(args.cpu_budget)
         thr = oracle.num_threads()
-        line["cpu_baseline"] = {"value": step_b / t_rep / 1e9, "unit": "GB/s", "cores": thr, "kind": "oracle",
-                                "sample": f"whole workload (scatter + decode), {reps} repetitions, "
+        line["cpu_baseline"] = {"value": (dbytes + scatter_bytes(S, H, D, elt)) / t_rep / 1e9, "unit": "GB/s",
+                                "cores": thr, "kind": "oracle",
+                                "sample": f"decode part of the step (scatter + decode), {reps} repetitions, "
                                           f"{t_rep * reps:.1f} s wall"}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -417,6 +556,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="llama13b",
+                    help="llama13b (the headline configuration) or another configuration")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU-oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

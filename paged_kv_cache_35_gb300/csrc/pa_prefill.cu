@@ -7,36 +7,47 @@
 // which already holds every earlier token and the chunk's own tokens.
 //
 // Design (ours, for one GB300):
-//  * One CTA per (128-query tile, head, chunk), 6 warps:
-//      warp 5  (loader)   TMA: the query tile once (3-D tensor map over
-//              [token][head][dim]) and, per 128-key tile, the K and V rows of
-//              the pages that hold those keys (2-D tensor map over the pool
-//              seen as [block*H*B + slot][dim]), into a 2-stage ring;
-//      warp 4  (MMA)      one thread issues tcgen05.mma (kind::f16, M=N=128,
-//              K=16 per instruction, fp32 accumulators in tensor memory):
-//              S_j = Q K_j^T into one of two TMEM score buffers, then
-//              O += P_j V_j into the TMEM output accumulator;
-//      warps 0-3 (softmax) thread i owns query row i = TMEM lane i: it reads
-//              its score row with tcgen05.ld, applies the causal / context
-//              mask, runs the online softmax, and writes its probability row
-//              into a shared-memory operand for the P V product as two
-//              16-bit parts, P = P_hi + P_lo (P_hi = P rounded to the input
-//              type, P_lo = the rounded remainder), and O += P_hi V + P_lo V.
-//              One 16-bit P would carry only 8 (bf16) or 11 (fp16) bits and
-//              its rounding alone moves a peaked row's output by ~2^-9 |v|;
-//              the two parts carry ~16 bits, at the cost of one more MMA group.
-//    S_{j+1} is issued before P_j V_j, so the softmax of tile j+1 overlaps
-//    the tensor-core work of tile j.
-//  * Operands are 128-byte-swizzled: K-major for Q, K and P; V is consumed
-//    MN-major (dims contiguous), straight from the pool layout.
-//  * The output accumulator is rescaled lazily: only when a row's running max
-//    grows by more than 2^8 (then O is read, scaled and written back in
-//    tensor memory); otherwise the stale max is kept, which is exact because
-//    the same max is used for the row sum.
-//  * Keys past the context, keys of pages whose table entry is bad, and keys
-//    past a query's position are masked; V rows that were not loaded or lie
-//    past the context are zeroed in shared memory so that stale or NaN bits
-//    cannot reach the P V product.
+//  * One CTA per (128-query tile, head, chunk), 10 warps:
+//      warp 9  (loader)  TMA: the query tile once (3-D tensor map over
+//              [token][head][dim]); per 128-key tile the K rows and the V
+//              rows of its pages into 3- and 2-stage rings (2-D tensor maps over
+//              the pool seen as [block*H*B + slot][dim]); pages outside the
+//              table are read at an out-of-range row, which the TMA fills
+//              with zeros;
+//      warp 8  (MMA)     one thread issues tcgen05.mma (kind::f16, M = N = 128,
+//              K = 16, fp32 accumulators in tensor memory): S(j) = Q K_j^T
+//              into one of two score buffers, and for each half h of the key
+//              tile O_h += P_h(j) V_h(j), with P_h(j) read back from the same
+//              buffer (A operand in tensor memory), into one of two output
+//              accumulators;
+//      warps 0-7 (softmax) two threads per query row (TMEM lane): warp w
+//              owns keys 64*(w/4) .. +63 of every key tile for the rows of
+//              lane quarter w%4, with its own running max, sum and output
+//              accumulator O_(w/4), so the two halves of a row never wait for
+//              each other; they merge by log-sum-exp once, at the end.  Each
+//              thread reads its 64 scores with one tcgen05.ld, masks (only
+//              tiles on the diagonal, at the context end or with a bad page),
+//              runs the online softmax, and writes P over its own 64 score
+//              columns with tcgen05.st as two 16-bit parts, P = P_hi + P_lo
+//              (P_hi = P rounded to the input type, P_lo = the rounded
+//              remainder), so that O_h += P_hi V + P_lo V carries ~16 bits of
+//              P: a single 16-bit P carries 8 (bf16) or 11 (fp16) bits, and its
+//              rounding alone moves a peaked row's output by ~2^-9 |v|.
+//    The MMA thread issues S(0), S(1), then per key tile j: P_0(j) V, P_1(j)
+//    V, S(j+2): the score buffer of tile j+1 is ready while the softmax of
+//    tile j runs.  An output accumulator is rescaled lazily (only when its
+//    half-row max grew by more than 2^8: it is read, scaled and written back
+//    in tensor memory); only then does the softmax of tile j wait for
+//    P_h(j-1) V, otherwise it overlaps it.
+//  * Operands in shared memory are 128-byte swizzled: K-major for Q and K;
+//    V is consumed MN-major (dims contiguous), straight from the pool layout.
+//  * Keys past the context or in a bad page, and keys past a query's
+//    position, are masked; V rows past the context are zeroed in shared
+//    memory before the product, so pool bits past a sequence's end (even NaN)
+//    cannot reach the output.
+//  * Work order: every CTA ranks the (chunk, query tile) pairs by their
+//    key-tile count, so the hardware's in-order dispatch starts the longest
+//    CTAs first.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -46,38 +57,46 @@
 
 namespace pa {
 
-constexpr int kPfRows = 128;   // query rows per CTA (MMA M)
+constexpr int kPfRows = 128;   // query rows per tile (MMA M)
 constexpr int kPfKeys = 128;   // keys per tile (N of S = Q K^T, K of O += P V)
 constexpr int kPfD = 128;      // head_dim
-constexpr int kPfThreads = 192;
-constexpr int kPfMmaWarp = 4;
-constexpr int kPfLoadWarp = 5;
+constexpr int kPfThreads = 320;
+constexpr int kPfMmaWarp = 8;
+constexpr int kPfLoadWarp = 9;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr uint32_t kHalfBytes = kPfRows * 64 * 2;  // 128 rows x 64 columns x 2 bytes
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;     // one 128 x 128 16-bit tile
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+// tensor-memory columns: two score buffers (later P) and the two half-row outputs
+__device__ __forceinline__ uint32_t tmem_s(int b) { return b ? 128u : 0u; }
+__device__ __forceinline__ uint32_t tmem_o(int h) { return h ? 384u : 256u; }
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;       // 2 stages
-constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;   // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;   // P_hi, then P_lo
-constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;             // kKStages stages
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;  // kVStages stages
+constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
 constexpr int kPfRankMax = 1024;  // (chunk, query tile) pairs ranked in-kernel
 
 struct PfBars {
   uint64_t q_full;
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2];      // per score buffer
+  uint64_t p_full[2][2];   // [half][buffer]: every row wrote P_h(j), buffer j % 2, one phase per use
+  uint64_t pv_done[2][2];  // per half: P_h(j) V complete, barrier j % 2, one phase per use
+  uint64_t v_zeroed;       // V rows past the context zeroed (last key tile)
+  uint64_t xbar[4];        // per lane quarter: both halves' (max, sum) written (end)
   uint64_t drain;
   uint32_t tmem_base;
-  uint32_t kv_mask[2];
+  float xm[2][kPfRows];  // half-row running max at the end: [half][row]
+  float xl[2][kPfRows];  // half-row sum at the end: [half][row]
   int abort_flag;
 };
 constexpr uint32_t kPfSmemBytes = kOffBar + sizeof(PfBars) + 1024;  // + alignment slack
+static_assert(kPfSmemBytes <= 227 * 1024, "shared memory beyond the per-CTA limit");
 
 struct PrefillArgs {
   void* out;
@@ -91,6 +110,7 @@ struct PrefillArgs {
   int num_blocks;
   int rows_per_load;  // min(block_size, 128)
   int rpl_shift;      // log2(rows_per_load)
+  int pool_rows;      // num_blocks * H * B: any row at or past it reads zeros
   int num_chunks;
   int qtiles;         // query tiles per chunk in the grid: ceil(max_q_len / 128)
   float qscale;       // scale * log2(e)
@@ -243,6 +263,43 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
   return (uint32_t)row * 128u + (uint32_t)((chunk ^ (row & 7)) << 4);
 }
 
+
+// tcgen05.mma with A read from tensor memory (the "TS" form): D += A B.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+
+// 64 consecutive fp32 columns of this thread's TMEM lane, load and wait in one
+// asm statement.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -257,17 +314,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int lane = threadIdx.x & 31;
   const int H = a.num_heads;
   const int B = a.block_size;
-  // Work order: the grid is 1-D over (chunk, query tile) pairs x heads.  The
-  // pairs are taken longest first (most key tiles), so the hardware's
-  // in-order dispatch schedules the long CTAs before the short ones.  Every
-  // CTA ranks the pairs itself from the chunk lengths (when there are at most
-  // kPfRankMax pairs; otherwise pairs go in their natural order).
+
+  // ---- which (chunk, query tile, head): longest first
   const int npairs = a.num_chunks * a.qtiles;
   const int my_rank = blockIdx.x / H;
   const int h = blockIdx.x - my_rank * H;
   int pair = my_rank;
   if (npairs <= kPfRankMax) {
-    int* cost = reinterpret_cast<int*>(gbase + kOffP);  // scratch, before the P buffers are used
+    int* cost = reinterpret_cast<int*>(gbase + kOffV);  // scratch, before any V tile is loaded
     int* chosen = cost + kPfRankMax;
     for (int e = threadIdx.x; e < npairs; e += blockDim.x) {
       const int cc = e / a.qtiles, tt = e - cc * a.qtiles;
@@ -291,26 +345,38 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   const int q0 = __ldg(a.cu_q_lens + c);
   const int n_c = __ldg(a.cu_q_lens + c + 1) - q0;
-  if (qt * kPfRows >= n_c) return;  // uniform across the CTA
+  const int row0 = qt * kPfRows;  // first query row of the tile within the chunk
+  if (row0 >= n_c) return;        // uniform across the CTA
   const int c0 = __ldg(a.ctx_before + c);
   const int ctx_total = c0 + n_c;
   if (c0 < 0 || n_c < 0 || (int64_t)ctx_total > (int64_t)a.max_blocks_per_seq * B) {
     if (threadIdx.x == 0) atomicOr(a.err_flag, PA_FLAG_BAD_LENGTH);
     return;
   }
-  const int last_row = min(qt * kPfRows + kPfRows - 1, n_c - 1);
-  const int n_kv = (c0 + last_row) / kPfKeys + 1;
+  const int rows = min(kPfRows, n_c - row0);
+  const int n_kv = (c0 + row0 + rows - 1) / kPfKeys + 1;
+  const bool need_zero = n_kv * kPfKeys > ctx_total;  // last key tile runs past the context
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.kv_full[i], 1);
-      mbar_init(&bars.kv_empty[i], 1);
-      mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_empty[i], 4);
-      mbar_init(&bars.p_full[i], 4);
-      mbar_init(&bars.pv_done[i], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
     }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
+    }
+    mbar_init(&bars.s_full[0], 1);
+    mbar_init(&bars.s_full[1], 1);
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(&bars.p_full[hh][0], 4);
+      mbar_init(&bars.p_full[hh][1], 4);
+      mbar_init(&bars.pv_done[hh][0], 1);
+      mbar_init(&bars.pv_done[hh][1], 1);
+    }
+    mbar_init(&bars.v_zeroed, 4);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars.xbar[q], 2);
     mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
     fence_barrier_init();
@@ -330,24 +396,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (warp == kPfLoadWarp) {
     // ---------------------------------------------------------------- loader
     const int rpl = a.rows_per_load;
-    const int loads = kPfKeys / rpl;  // sub-blocks per key tile (1..8)
+    const int loads = kPfKeys / rpl;  // page pieces per key tile (1..8)
     const int32_t* trow = a.block_tables + (size_t)c * a.max_blocks_per_seq;
-    int issued = 0;
+    int k_issued = 0, v_issued = 0;
     if (lane == 0) {
       mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
-      tma_load_3d(base + kOffQ, &tm_q, 0, h, q0 + qt * kPfRows, &bars.q_full);
-      tma_load_3d(base + kOffQ + kHalfBytes, &tm_q, 64, h, q0 + qt * kPfRows, &bars.q_full);
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_3d(base + kOffQ + hf * kHalfBytes, &tm_q, hf * 64, h, q0 + row0, &bars.q_full);
     }
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&bars.kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, a.err_flag);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const int key0 = j * kPfKeys;
-      int row = 0;
+    int prev_row = 0;  // this lane's page row of the previous key tile (its V is loaded one step later)
+    for (int t = 0; t <= n_kv; ++t) {
+      int row = a.pool_rows;  // out of range: the TMA fills zeros
       bool have = false;
-      if (lane < loads) {
-        const int pos = key0 + lane * rpl;
+      if (t < n_kv && lane < loads) {
+        const int pos = t * kPfKeys + lane * rpl;
         if (pos < ctx_total) {
           const int32_t blk = __ldg(trow + pos / B);
           if (blk >= 0 && blk < a.num_blocks) {
@@ -359,118 +421,153 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       const uint32_t mask = __ballot_sync(0xffffffffu, have);
-      if (lane == 0) {
-        bars.kv_mask[st] = mask;
-        const uint32_t bytes = (uint32_t)__popc(mask) * (uint32_t)rpl * 128u * 4u;
-        mbar_arrive_expect_tx(&bars.kv_full[st], bytes);
-      }
-      for (int r = 0; r < loads; ++r) {
-        const int rr = __shfl_sync(0xffffffffu, row, r);
-        if (lane == 0 && ((mask >> r) & 1u)) {
-          const uint32_t off = (uint32_t)r * rpl * 128u;
-          const uint32_t kdst = base + kOffK + st * kTileBytes + off;
-          const uint32_t vdst = base + kOffV + st * kTileBytes + off;
-          tma_load_2d(kdst, &tm_k, 0, rr, &bars.kv_full[st]);
-          tma_load_2d(kdst + kHalfBytes, &tm_k, 64, rr, &bars.kv_full[st]);
-          tma_load_2d(vdst, &tm_v, 0, rr, &bars.kv_full[st]);
-          tma_load_2d(vdst + kHalfBytes, &tm_v, 64, rr, &bars.kv_full[st]);
+      int ok = 1;
+      if (t < n_kv) {  // K of tile t
+        const int st = t % kKStages;
+        if (lane == 0) ok = mbar_wait(&bars.k_empty[st], ((t / kKStages) & 1) ^ 1, abort_flag, a.err_flag);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars.k_full[st], kTileBytes);
+        for (int r = 0; r < loads; ++r) {
+          const int rr = __shfl_sync(0xffffffffu, row, r);
+          if (lane == 0) {
+            const uint32_t dst = base + kOffK + st * kTileBytes + (uint32_t)r * rpl * 128u;
+            tma_load_2d(dst, &tm_k, 0, rr, &bars.k_full[st]);
+            tma_load_2d(dst + kHalfBytes, &tm_k, 64, rr, &bars.k_full[st]);
+          }
         }
+        ++k_issued;
       }
-      ++issued;
+      if (t >= 1) {  // V of tile t - 1
+        const int tv = t - 1;
+        const int st = tv % kVStages;
+        if (lane == 0) ok = mbar_wait(&bars.v_empty[st], ((tv / kVStages) & 1) ^ 1, abort_flag, a.err_flag);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars.v_full[st], kTileBytes);
+        for (int r = 0; r < loads; ++r) {
+          const int rr = __shfl_sync(0xffffffffu, prev_row, r);
+          if (lane == 0) {
+            const uint32_t dst = base + kOffV + st * kTileBytes + (uint32_t)r * rpl * 128u;
+            tma_load_2d(dst, &tm_v, 0, rr, &bars.v_full[st]);
+            tma_load_2d(dst + kHalfBytes, &tm_v, 64, rr, &bars.v_full[st]);
+          }
+        }
+        ++v_issued;
+      }
+      prev_row = row;
     }
     if (lane == 0 && *abort_flag) {  // let in-flight tiles land before exit
       mbar_wait_drain(&bars.q_full, 0);
-      for (int jj = max(0, issued - 2); jj < issued; ++jj) mbar_wait_drain(&bars.kv_full[jj & 1], (jj >> 1) & 1);
+      for (int t = max(0, k_issued - kKStages); t < k_issued; ++t)
+        mbar_wait_drain(&bars.k_full[t % kKStages], (t / kKStages) & 1);
+      for (int t = max(0, v_issued - kVStages); t < v_issued; ++t)
+        mbar_wait_drain(&bars.v_full[t % kVStages], (t / kVStages) & 1);
     }
   } else if (warp == kPfMmaWarp) {
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
       bool ok = mbar_wait(&bars.q_full, 0, abort_flag, a.err_flag);
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int st = j & 1;
-          ok = mbar_wait(&bars.kv_full[st], (j >> 1) & 1, abort_flag, a.err_flag) &&
-               mbar_wait(&bars.s_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, a.err_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kb = base + kOffK + st * kTileBytes;
+      const uint64_t qdesc = smem_desc_sw128(base + kOffQ, 16, 1024);
+      // S(t) = Q K_t^T into score buffer t % 2
+      auto issue_s = [&](int t) -> bool {
+        if (!mbar_wait(&bars.k_full[t % kKStages], (t / kKStages) & 1, abort_flag, a.err_flag)) return false;
+        tc_fence_after();
+        // descriptors advance by adding (byte offset >> 4) to the start-address field
+        const uint64_t kdesc = smem_desc_sw128(base + kOffK + (t % kKStages) * kTileBytes, 16, 1024);
+        const uint32_t d = tmem + tmem_s(t & 1);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            umma_f16(tmem + (st ? kTmemS1 : kTmemS0), smem_desc_sw128(base + kOffQ + koff, 16, 1024),
-                     smem_desc_sw128(kb + koff, 16, 1024), a.idesc_s, kk > 0);
-          }
-          umma_commit(&bars.s_full[st]);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t koff = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          umma_f16(d, qdesc + koff, kdesc + koff, a.idesc_s, kk > 0);
         }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int st = jj & 1;
-          ok = mbar_wait(&bars.p_full[st], (jj >> 1) & 1, abort_flag, a.err_flag);
+        umma_commit(&bars.s_full[t & 1]);
+        umma_commit(&bars.k_empty[t % kKStages]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n_kv > 1) ok = issue_s(1);
+      for (int t = 0; ok && t < n_kv; ++t) {
+        ok = mbar_wait(&bars.v_full[t % kVStages], (t / kVStages) & 1, abort_flag, a.err_flag);
+        if (ok && need_zero && t == n_kv - 1) ok = mbar_wait(&bars.v_zeroed, 0, abort_flag, a.err_flag);
+        const uint64_t vdesc = smem_desc_sw128(base + kOffV + (t % kVStages) * kTileBytes, kHalfBytes, 1024);
+        const uint32_t pb = tmem + tmem_s(t & 1);
+        const uint32_t first = t > 0 ? 1u : 0u;
+#pragma unroll
+        for (int hh = 0; hh < 2 && ok; ++hh) {  // O_h += P_h V_h: keys 64h .. 64h+63 of the tile
+          ok = mbar_wait(&bars.p_full[hh][t & 1], (t >> 1) & 1, abort_flag, a.err_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t vb = base + kOffV + st * kTileBytes;
 #pragma unroll
           for (int part = 0; part < 2; ++part) {  // P_hi V, then P_lo V
-            const uint32_t pb = base + kOffP + part * kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t poff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-              umma_f16(tmem + kTmemO, smem_desc_sw128(pb + poff, 16, 1024),
-                       smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), a.idesc_pv,
-                       (jj > 0 || kk > 0 || part > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              umma_f16_ts(tmem + tmem_o(hh), pb + hh * 64 + part * 32 + kk * 8,
+                          vdesc + (((hh * 4 + kk) * 2048) >> 4), a.idesc_pv, (kk > 0 || part > 0) ? 1u : first);
             }
           }
-          umma_commit(&bars.pv_done[st]);
-          umma_commit(&bars.kv_empty[st]);
+          umma_commit(&bars.pv_done[hh][t & 1]);
         }
+        if (!ok) break;
+        umma_commit(&bars.v_empty[t % kVStages]);
+        if (t + 2 < n_kv) ok = issue_s(t + 2);  // after P(t) V in issue order: its buffer is free then
       }
       // every issued MMA has finished before tensor memory is released
       umma_commit(&bars.drain);
       mbar_wait_drain(&bars.drain, 0);
     }
-  } else {
-    // ---------------------------------------------------------------- softmax warps 0-3
-    const int row = threadIdx.x;  // query row within the tile = TMEM lane
-    const int qrow = qt * kPfRows + row;
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------- softmax warps
+    const int quarter = warp & 3;      // TMEM lane quarter this warp may access
+    const int half = warp >> 2;        // columns 64*half .. 64*half+63
+    const int r = quarter * 32 + lane; // query row within the tile = TMEM lane
+    const int qrow = row0 + r;
     const int pos = c0 + qrow;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const int tile_first_pos = c0 + row0;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t full_mask = (1u << (kPfKeys / a.rows_per_load)) - 1u;
+    const int col0 = half * 64;
+    const uint32_t s_half = lane_addr + col0;  // + score buffer: this half's 64 columns
+    const uint32_t o_mine = lane_addr + tmem_o(half);
+    // Page pieces of a key tile whose table entry is usable: the loader
+    // zero-fills the others and they are masked here.  Each lane < pieces
+    // reads one table entry, one tile ahead so the load latency is hidden.
+    const int rpl = a.rows_per_load;
+    const int pieces = kPfKeys / rpl;
+    const int32_t* trow = a.block_tables + (size_t)c * a.max_blocks_per_seq;
+    auto piece_entry = [&](int t) -> int32_t {
+      const int p = t * kPfKeys + lane * rpl;
+      return (t < n_kv && lane < pieces && p < ctx_total) ? __ldg(trow + p / B) : -1;
+    };
+    int32_t entry_next = piece_entry(0);
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      // kv_full: the loader's mask for this tile and the V rows are read below
-      ok = mbar_wait(&bars.s_full[st], (j >> 1) & 1, abort_flag, a.err_flag) &&
-           mbar_wait(&bars.kv_full[st], (j >> 1) & 1, abort_flag, a.err_flag);
+    for (int t = 0; t < n_kv; ++t) {
+      const int sb = t & 1;
+      const uint32_t kmask = __ballot_sync(0xffffffffu, entry_next >= 0 && entry_next < a.num_blocks);
+      entry_next = piece_entry(t + 1);
+      ok = mbar_wait(&bars.s_full[sb], (t >> 1) & 1, abort_flag, a.err_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[kPfKeys];
-      tmem_ld128(lane_addr + (st ? kTmemS1 : kTmemS0), s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_empty[st]);
+      float s[64];
+      tmem_ld64(s_half + tmem_s(sb), s);
 
-      const int key0 = j * kPfKeys;
-      const uint32_t kmask = bars.kv_mask[st];
-      // interior tile: every key precedes every query of the tile, lies in the
-      // context and was loaded -- no masking at all
-      const bool interior = key0 + kPfKeys - 1 <= c0 + qt * kPfRows && key0 + kPfKeys <= ctx_total &&
-                            kmask == full_mask;
+      const int key0 = t * kPfKeys;
+      const bool interior = key0 + kPfKeys - 1 <= tile_first_pos && key0 + kPfKeys <= ctx_total && kmask == full_mask;
       if (!interior) {
         const int lim = min(pos, ctx_total - 1) - key0;  // last admissible column of this row
 #pragma unroll
-        for (int col = 0; col < kPfKeys; ++col) {
+        for (int i = 0; i < 64; ++i) {
+          const int col = col0 + i;
           const bool valid = col <= lim && ((kmask >> (col >> a.rpl_shift)) & 1u);
-          s[col] = valid ? s[col] : -INFINITY;
+          s[i] = valid ? s[i] : -INFINITY;
         }
       }
       float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int col = 4; col < kPfKeys; ++col) mx4[col & 3] = fmaxf(mx4[col & 3], s[col]);
+      for (int i = 4; i < 64; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
       const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.qscale;  // qscale > 0
       const float m_new = fmaxf(m_used, rmax);
       const bool resc = m_new > m_used + kRescaleThreshold;  // also true when m_used is -inf
@@ -479,104 +576,120 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       l *= alpha;
       const float mref = (m_next == -INFINITY) ? 0.f : m_next;
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t hw[32], lw[32];
 #pragma unroll
-      for (int col = 0; col < kPfKeys; ++col) {
-        s[col] = ex2_approx(fmaf(s[col], a.qscale, -mref));
-        sum4[col & 3] += s[col];
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = ex2_approx(fmaf(s[2 * e], a.qscale, -mref));
+        const float p1 = ex2_approx(fmaf(s[2 * e + 1], a.qscale, -mref));
+        sum4[e & 3] += p0 + p1;
+        split2<T>(p0, p1, hw[e], lw[e]);
       }
       l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      // P_{j-1} V_{j-1} must be complete: it reads the P buffer written below
-      // and it is the last product O holds before a rescale
-      if (j > 0) {
-        ok = mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, a.err_flag);
+      // This half's columns of the buffer still hold P_h(t-2): wait for
+      // P_h(t-2) V.  A rescale of O_h also needs P_h(t-1) V in it.
+      const bool any_resc = t > 0 && __any_sync(0xffffffffu, resc);
+      if (t >= 2) ok = mbar_wait(&bars.pv_done[half][t & 1], ((t - 2) >> 1) & 1, abort_flag, a.err_flag);
+      if (ok && any_resc)
+        ok = mbar_wait(&bars.pv_done[half][(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, a.err_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // P_h over this half's scores: P_hi in its first 32 words, P_lo in the next 32
+      const uint32_t pw = s_half + tmem_s(sb);
+      tmem_st16(pw, hw);
+      tmem_st16(pw + 16, hw + 16);
+      tmem_st16(pw + 32, lw);
+      tmem_st16(pw + 48, lw + 16);
+      if (any_resc) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(o_mine + cc * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(o_mine + cc * 32, o);
+        }
+      }
+      tmem_st_wait();
+      if (half == 0 && need_zero && t == n_kv - 1) {
+        // zero the V rows of this last key tile that lie past the context
+        ok = mbar_wait(&bars.v_full[t % kVStages], (t / kVStages) & 1, abort_flag, a.err_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-      }
-      uint8_t* phi = gbase + kOffP;
-      uint8_t* plo = gbase + kOffP + kTileBytes;
+        if (key0 + r >= ctx_total) {
+          uint8_t* vbuf = gbase + kOffV + (t % kVStages) * kTileBytes;
+          const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const float* src = s + half * 64 + ch * 8;
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split2<T>(src[2 * e], src[2 * e + 1], hw[e], lw[e]);
-          const uint32_t off = half * kHalfBytes + sw128_offset(row, ch);
-          *reinterpret_cast<uint4*>(phi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(plo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          for (int ch = 0; ch < 8; ++ch) {
+            *reinterpret_cast<uint4*>(vbuf + r * 128 + ch * 16) = z;
+            *reinterpret_cast<uint4*>(vbuf + kHalfBytes + r * 128 + ch * 16) = z;
+          }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.v_zeroed);
       }
-      // key row `row` of V: zero it if it was not loaded or lies past the context
-      const int key = key0 + row;
-      if (key >= ctx_total || !((kmask >> (row >> a.rpl_shift)) & 1u)) {
-        uint8_t* vbuf = gbase + kOffV + st * kTileBytes;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          *reinterpret_cast<uint4*>(vbuf + row * 128 + ch * 16) = z;
-          *reinterpret_cast<uint4*>(vbuf + kHalfBytes + row * 128 + ch * 16) = z;
-        }
-      }
-      // rescale O in tensor memory when the running max moved (after P is
-      // stored, so the probabilities are no longer held in registers)
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
-          tmem_ld32(lane_addr + kTmemO + cc * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(lane_addr + kTmemO + cc * 32, o);
-        }
-        tmem_st_wait();
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full[st]);
+      if (lane == 0) mbar_arrive(&bars.p_full[half][sb]);
       m_used = m_next;
     }
-    if (ok) {
-      const int jl = n_kv - 1;
-      ok = mbar_wait(&bars.pv_done[jl & 1], (jl >> 1) & 1, abort_flag, a.err_flag);
-    }
+    // ---- epilogue: merge the two half-rows (log-sum-exp), write this half's 64 output columns
+    if (ok) ok = mbar_wait(&bars.pv_done[half][(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, abort_flag, a.err_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    bars.xm[half][r] = m_used;
+    bars.xl[half][r] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.xbar[quarter]);
+    if (ok) ok = mbar_wait(&bars.xbar[quarter], 0, abort_flag, a.err_flag);
+    // the partner's output must be complete too before its columns are read
+    if (ok) ok = mbar_wait(&bars.pv_done[1 - half][(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, abort_flag, a.err_flag);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float m0 = bars.xm[0][r], m1 = bars.xm[1][r];
+      const float M = fmaxf(m0, m1);
+      const float w0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - M);
+      const float w1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
+      const float lt = w0 * bars.xl[0][r] + w1 * bars.xl[1][r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float c0w = w0 * inv, c1w = w1 * inv;
       const bool store = qrow < n_c;
-      const size_t obase = ((size_t)(q0 + qrow) * H + h) * kPfD;
+      const size_t obase = ((size_t)(q0 + qrow) * H + h) * kPfD + col0;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
+        float oa[32], ob[32];
+        tmem_ld32(lane_addr + tmem_o(0) + col0 + cc * 32, oa);
+        tmem_ld32(lane_addr + tmem_o(1) + col0 + cc * 32, ob);
         float o[32];
-        tmem_ld32(lane_addr + kTmemO + cc * 32, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = c0w * oa[i] + c1w * ob[i];
         if (store) {
           if (a.out_dtype == PA_F32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + obase + cc * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
           } else {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + obase + cc * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float* x = o + 8 * i;
-              uint4 v;
+              const float* v = o + 8 * i;
+              uint4 w;
               if (a.out_dtype == PA_BF16) {
-                v.x = pack2<__nv_bfloat16>(x[0] * inv, x[1] * inv);
-                v.y = pack2<__nv_bfloat16>(x[2] * inv, x[3] * inv);
-                v.z = pack2<__nv_bfloat16>(x[4] * inv, x[5] * inv);
-                v.w = pack2<__nv_bfloat16>(x[6] * inv, x[7] * inv);
+                w.x = pack2<__nv_bfloat16>(v[0], v[1]);
+                w.y = pack2<__nv_bfloat16>(v[2], v[3]);
+                w.z = pack2<__nv_bfloat16>(v[4], v[5]);
+                w.w = pack2<__nv_bfloat16>(v[6], v[7]);
               } else {
-                v.x = pack2<__half>(x[0] * inv, x[1] * inv);
-                v.y = pack2<__half>(x[2] * inv, x[3] * inv);
-                v.z = pack2<__half>(x[4] * inv, x[5] * inv);
-                v.w = pack2<__half>(x[6] * inv, x[7] * inv);
+                w.x = pack2<__half>(v[0], v[1]);
+                w.y = pack2<__half>(v[2], v[3]);
+                w.z = pack2<__half>(v[4], v[5]);
+                w.w = pack2<__half>(v[6], v[7]);
               }
-              dst[i] = v;
+              dst[i] = w;
             }
           }
         }
@@ -685,6 +798,7 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
   a.num_blocks = num_blocks;
   a.rows_per_load = rows_per_load;
   a.rpl_shift = 31 - __builtin_clz((unsigned)rows_per_load);
+  a.pool_rows = (int)pool_rows;
   a.qscale = scale * 1.4426950408889634f;
   const uint32_t fmt = dtype == PA_BF16 ? 1u : 0u;
   a.idesc_s = make_idesc(fmt, false);

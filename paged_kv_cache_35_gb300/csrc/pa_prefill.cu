@@ -7,12 +7,15 @@
 // which already holds every earlier token and the chunk's own tokens.
 //
 // Design (ours, for one GB300):
-//  * One CTA per (128-query tile, head, chunk), 10 warps:
-//      warp 9  (loader)  TMA: the query tile once (3-D tensor map over
-//              [token][head][dim]); per 128-key tile the K rows and the V
-//              rows of its pages into 3- and 2-stage rings (2-D tensor maps over
-//              the pool seen as [block*H*B + slot][dim]); pages outside the
-//              table are read at an out-of-range row, which the TMA fills
+//  * Persistent: one CTA per SM (its shared and tensor memory allow one),
+//    each walking a list of items -- (128-query tile, chunk, head) -- in
+//    longest-first order, 10 warps:
+//      warp 9  (loader)  TMA: per item the query tile (3-D tensor map over
+//              [token][head][dim]) once the previous item's last S = Q K^T is
+//              done with the buffer; per 128-key tile the K rows and the V
+//              rows of its pages into 2- and 3-stage rings (2-D tensor maps
+//              over the pool seen as [block*H*B + slot][dim]); pages outside
+//              the table are read at an out-of-range row, which the TMA fills
 //              with zeros;
 //      warp 8  (MMA)     one thread issues tcgen05.mma (kind::f16, M = N = 128,
 //              K = 16, fp32 accumulators in tensor memory): S(j) = Q K_j^T
@@ -24,21 +27,23 @@
 //              owns keys 64*(w/4) .. +63 of every key tile for the rows of
 //              lane quarter w%4, with its own running max, sum and output
 //              accumulator O_(w/4), so the two halves of a row never wait for
-//              each other; they merge by log-sum-exp once, at the end.  Each
-//              thread reads its 64 scores with one tcgen05.ld, masks (only
-//              tiles on the diagonal, at the context end or with a bad page),
-//              runs the online softmax, and writes P over its own 64 score
-//              columns with tcgen05.st as two 16-bit parts, P = P_hi + P_lo
-//              (P_hi = P rounded to the input type, P_lo = the rounded
-//              remainder), so that O_h += P_hi V + P_lo V carries ~16 bits of
-//              P: a single 16-bit P carries 8 (bf16) or 11 (fp16) bits, and its
-//              rounding alone moves a peaked row's output by ~2^-9 |v|.
+//              each other; they merge by log-sum-exp once, at the end of the
+//              item.  Each thread reads its 64 scores with one tcgen05.ld,
+//              masks (only tiles on the diagonal, at the context end or with a
+//              bad page), runs the online softmax, and writes P over its own 64
+//              score columns with tcgen05.st as two 16-bit parts, P = P_hi +
+//              P_lo (P_hi = P in the input type, P_lo = the remainder in the
+//              input type), so that O_h += P_hi V + P_lo V carries ~16 bits
+//              of P: a single 16-bit P carries 8 (bf16) or 11 (fp16) bits, and
+//              its rounding alone moves a peaked row's output by ~2^-9 |v|.
 //    The MMA thread issues S(0), S(1), then per key tile j: P_0(j) V, P_1(j)
 //    V, S(j+2): the score buffer of tile j+1 is ready while the softmax of
 //    tile j runs.  An output accumulator is rescaled lazily (only when its
 //    half-row max grew by more than 2^8: it is read, scaled and written back
 //    in tensor memory); only then does the softmax of tile j wait for
-//    P_h(j-1) V, otherwise it overlaps it.
+//    P_h(j-1) V, otherwise it overlaps it.  Ring stages and barrier phases
+//    follow running per-CTA counters, so the next item's query load and first
+//    two S products overlap the current item's last tiles and epilogue.
 //  * Operands in shared memory are 128-byte swizzled: K-major for Q and K;
 //    V is consumed MN-major (dims contiguous), straight from the pool layout.
 //  * Keys past the context or in a bad page, and keys past a query's
@@ -46,8 +51,8 @@
 //    memory before the product, so pool bits past a sequence's end (even NaN)
 //    cannot reach the output.
 //  * Work order: every CTA ranks the (chunk, query tile) pairs by their
-//    key-tile count, so the hardware's in-order dispatch starts the longest
-//    CTAs first.
+//    key-tile count; the items (pairs times heads) are dealt to the CTAs in
+//    that order, forward and backward in alternate rounds.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -63,8 +68,8 @@ constexpr int kPfD = 128;      // head_dim
 constexpr int kPfThreads = 320;
 constexpr int kPfMmaWarp = 8;
 constexpr int kPfLoadWarp = 9;
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
 constexpr uint32_t kHalfBytes = kPfRows * 64 * 2;  // 128 rows x 64 columns x 2 bytes
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;     // one 128 x 128 16-bit tile
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
@@ -81,19 +86,21 @@ constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
 constexpr int kPfRankMax = 1024;  // (chunk, query tile) pairs ranked in-kernel
 
 struct PfBars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;  // query tile loaded / its last S = Q K^T done
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2];      // per score buffer
   uint64_t p_full[2][2];   // [half][buffer]: every row wrote P_h(j), buffer j % 2, one phase per use
   uint64_t pv_done[2][2];  // per half: P_h(j) V complete, barrier j % 2, one phase per use
   uint64_t v_zeroed;       // V rows past the context zeroed (last key tile)
-  uint64_t xbar[4];        // per lane quarter: both halves' (max, sum) written (end)
+  uint64_t xbar[4];        // per lane quarter: both halves' (max, sum) written (end of an item)
+  uint64_t o_free;         // every softmax warp has read the output accumulators (end of an item)
   uint64_t drain;
   uint32_t tmem_base;
   float xm[2][kPfRows];  // half-row running max at the end: [half][row]
   float xl[2][kPfRows];  // half-row sum at the end: [half][row]
   int abort_flag;
+  uint16_t order[kPfRankMax];  // (chunk, query tile) pairs, longest first
 };
 constexpr uint32_t kPfSmemBytes = kOffBar + sizeof(PfBars) + 1024;  // + alignment slack
 static_assert(kPfSmemBytes <= 227 * 1024, "shared memory beyond the per-CTA limit");
@@ -250,11 +257,15 @@ __device__ __forceinline__ void split2<__half>(float x, float y, uint32_t& hi, u
 }
 template <>
 __device__ __forceinline__ void split2<__nv_bfloat16>(float x, float y, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 r = __floats2bfloat162_rn(x - hf.x, y - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&r);
+  // bf16 is the upper half of an fp32: hi keeps the upper 16 bits of x and y
+  // (truncation), the remainder x - hi is exact in fp32 and is truncated the
+  // same way.  hi + lo is within 2^-15 of x relative; no conversion
+  // instructions, only bit selects and two subtractions.
+  const uint32_t xb = __float_as_uint(x), yb = __float_as_uint(y);
+  const float rx = x - __uint_as_float(xb & 0xffff0000u);
+  const float ry = y - __uint_as_float(yb & 0xffff0000u);
+  hi = __byte_perm(xb, yb, 0x7632);
+  lo = __byte_perm(__float_as_uint(rx), __float_as_uint(ry), 0x7632);
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
@@ -300,6 +311,58 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// One unit of work: a 128-row query tile of one chunk, for one head.
+struct PfItem {
+  int c, h;         // chunk, head
+  int q0, n_c;      // chunk's first row in q / out, its query count
+  int row0, rows;   // tile's first query row within the chunk, rows in the tile
+  int c0, ctx_total;
+  int n_kv;         // key tiles the tile's queries see
+  bool need_zero;   // the last key tile runs past the context
+};
+
+enum { kItemRun = 0, kItemEmpty = 1, kItemBadLength = 2 };
+
+// Item at position `pos` of the longest-first list.  The list is (chunk,
+// query tile) pairs in `order` (or, past kPfRankMax pairs, later query tiles
+// first), each expanded over the heads.
+__device__ __forceinline__ int pf_item(const PrefillArgs& a, const uint16_t* order, int npairs, int pos, PfItem& it) {
+  const int H = a.num_heads;
+  const int rank = pos / H;
+  it.h = pos - rank * H;
+  int c, qt;
+  if (npairs <= kPfRankMax) {
+    const int pair = order[rank];
+    c = pair / a.qtiles;
+    qt = pair - c * a.qtiles;
+  } else {
+    const int from_end = rank / a.num_chunks;
+    c = rank - from_end * a.num_chunks;
+    qt = a.qtiles - 1 - from_end;
+  }
+  it.c = c;
+  it.q0 = __ldg(a.cu_q_lens + c);
+  it.n_c = __ldg(a.cu_q_lens + c + 1) - it.q0;
+  it.row0 = qt * kPfRows;
+  if (it.row0 >= it.n_c) return kItemEmpty;
+  it.c0 = __ldg(a.ctx_before + c);
+  it.ctx_total = it.c0 + it.n_c;
+  if (it.c0 < 0 || (int64_t)it.ctx_total > (int64_t)a.max_blocks_per_seq * a.block_size) return kItemBadLength;
+  it.rows = min(kPfRows, it.n_c - it.row0);
+  it.n_kv = (it.c0 + it.row0 + it.rows - 1) / kPfKeys + 1;
+  it.need_zero = it.n_kv * kPfKeys > it.ctx_total;
+  return kItemRun;
+}
+
+// Position of this CTA's round-r item in the longest-first list: rounds go
+// forward and backward over the CTAs in turn (CTA b takes b, 2G-1-b, 2G+b,
+// ...), so the CTA that drew the shortest item of one round draws the longest
+// of the next.
+__device__ __forceinline__ long long pf_round_pos(int r) {
+  const int G = gridDim.x, b = blockIdx.x;
+  return (long long)r * G + ((r & 1) ? (G - 1 - b) : b);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -314,15 +377,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int lane = threadIdx.x & 31;
   const int H = a.num_heads;
   const int B = a.block_size;
-
-  // ---- which (chunk, query tile, head): longest first
   const int npairs = a.num_chunks * a.qtiles;
-  const int my_rank = blockIdx.x / H;
-  const int h = blockIdx.x - my_rank * H;
-  int pair = my_rank;
+  const long long n_items = (long long)npairs * H;
+
+  // ---- rank the (chunk, query tile) pairs by key-tile count, longest first
   if (npairs <= kPfRankMax) {
     int* cost = reinterpret_cast<int*>(gbase + kOffV);  // scratch, before any V tile is loaded
-    int* chosen = cost + kPfRankMax;
     for (int e = threadIdx.x; e < npairs; e += blockDim.x) {
       const int cc = e / a.qtiles, tt = e - cc * a.qtiles;
       const int nq = __ldg(a.cu_q_lens + cc + 1) - __ldg(a.cu_q_lens + cc);
@@ -334,31 +394,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int ke = cost[e];
       int rank = 0;
       for (int f = 0; f < npairs; ++f) rank += (cost[f] > ke) || (cost[f] == ke && f < e);
-      if (rank == my_rank) chosen[0] = e;
+      bars.order[rank] = (uint16_t)e;
     }
-    __syncthreads();
-    pair = chosen[0];
-    __syncthreads();
   }
-  const int c = pair / a.qtiles;
-  const int qt = pair - c * a.qtiles;
-
-  const int q0 = __ldg(a.cu_q_lens + c);
-  const int n_c = __ldg(a.cu_q_lens + c + 1) - q0;
-  const int row0 = qt * kPfRows;  // first query row of the tile within the chunk
-  if (row0 >= n_c) return;        // uniform across the CTA
-  const int c0 = __ldg(a.ctx_before + c);
-  const int ctx_total = c0 + n_c;
-  if (c0 < 0 || n_c < 0 || (int64_t)ctx_total > (int64_t)a.max_blocks_per_seq * B) {
-    if (threadIdx.x == 0) atomicOr(a.err_flag, PA_FLAG_BAD_LENGTH);
-    return;
-  }
-  const int rows = min(kPfRows, n_c - row0);
-  const int n_kv = (c0 + row0 + rows - 1) / kPfKeys + 1;
-  const bool need_zero = n_kv * kPfKeys > ctx_total;  // last key tile runs past the context
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bars.k_full[i], 1);
       mbar_init(&bars.k_empty[i], 1);
@@ -376,6 +418,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&bars.pv_done[hh][1], 1);
     }
     mbar_init(&bars.v_zeroed, 4);
+    mbar_init(&bars.o_free, 8);
     for (int q = 0; q < 4; ++q) mbar_init(&bars.xbar[q], 2);
     mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
@@ -392,123 +435,165 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort_flag;
+  const uint16_t* order = bars.order;
 
+  // Every role walks the same item list.  Ring stages and barrier phases
+  // follow running counters: g = key tiles of this CTA's earlier items (the
+  // global index of a key tile is g + t), k = items run so far.
   if (warp == kPfLoadWarp) {
     // ---------------------------------------------------------------- loader
     const int rpl = a.rows_per_load;
     const int loads = kPfKeys / rpl;  // page pieces per key tile (1..8)
-    const int32_t* trow = a.block_tables + (size_t)c * a.max_blocks_per_seq;
-    int k_issued = 0, v_issued = 0;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
-      for (int hf = 0; hf < 2; ++hf)
-        tma_load_3d(base + kOffQ + hf * kHalfBytes, &tm_q, hf * 64, h, q0 + row0, &bars.q_full);
+    int g = 0, k = 0, k_issued = 0, v_issued = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const long long ipos = pf_round_pos(r);
+      if (ipos >= n_items) break;
+      PfItem it;
+      const int st = pf_item(a, order, npairs, (int)ipos, it);
+      if (st == kItemBadLength && lane == 0) atomicOr(a.err_flag, PA_FLAG_BAD_LENGTH);
+      if (st != kItemRun) continue;
+      const int32_t* trow = a.block_tables + (size_t)it.c * a.max_blocks_per_seq;
+      int wok = 1;
+      if (lane == 0) {  // the query tile, once the previous item's last S = Q K^T is done with the buffer
+        wok = mbar_wait(&bars.q_empty, (k & 1) ^ 1, abort_flag, a.err_flag);
+        if (wok) {
+          mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(base + kOffQ + hf * kHalfBytes, &tm_q, hf * 64, it.h, it.q0 + it.row0, &bars.q_full);
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, wok, 0)) break;
+      int prev_row = 0;  // this lane's page row of the previous key tile (its V is loaded one step later)
+      for (int t = 0; t <= it.n_kv; ++t) {
+        int row = a.pool_rows;  // out of range: the TMA fills zeros
+        if (t < it.n_kv && lane < loads) {
+          const int pos = t * kPfKeys + lane * rpl;
+          if (pos < it.ctx_total) {
+            const int32_t blk = __ldg(trow + pos / B);
+            if (blk >= 0 && blk < a.num_blocks) {
+              row = (blk * H + it.h) * B + pos % B;
+            } else {
+              atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
+            }
+          }
+        }
+        int wk = 1;
+        if (t < it.n_kv) {  // K of tile t
+          const int x = g + t;
+          const int stg = x % kKStages;
+          if (lane == 0) wk = mbar_wait(&bars.k_empty[stg], ((x / kKStages) & 1) ^ 1, abort_flag, a.err_flag);
+          if (!__shfl_sync(0xffffffffu, wk, 0)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&bars.k_full[stg], kTileBytes);
+          for (int pc = 0; pc < loads; ++pc) {
+            const int rr = __shfl_sync(0xffffffffu, row, pc);
+            if (lane == 0) {
+              const uint32_t dst = base + kOffK + stg * kTileBytes + (uint32_t)pc * rpl * 128u;
+              tma_load_2d(dst, &tm_k, 0, rr, &bars.k_full[stg]);
+              tma_load_2d(dst + kHalfBytes, &tm_k, 64, rr, &bars.k_full[stg]);
+            }
+          }
+          ++k_issued;
+        }
+        if (t >= 1) {  // V of tile t - 1
+          const int x = g + t - 1;
+          const int stg = x % kVStages;
+          if (lane == 0) wk = mbar_wait(&bars.v_empty[stg], ((x / kVStages) & 1) ^ 1, abort_flag, a.err_flag);
+          if (!__shfl_sync(0xffffffffu, wk, 0)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&bars.v_full[stg], kTileBytes);
+          for (int pc = 0; pc < loads; ++pc) {
+            const int rr = __shfl_sync(0xffffffffu, prev_row, pc);
+            if (lane == 0) {
+              const uint32_t dst = base + kOffV + stg * kTileBytes + (uint32_t)pc * rpl * 128u;
+              tma_load_2d(dst, &tm_v, 0, rr, &bars.v_full[stg]);
+              tma_load_2d(dst + kHalfBytes, &tm_v, 64, rr, &bars.v_full[stg]);
+            }
+          }
+          ++v_issued;
+        }
+        prev_row = row;
+      }
+      g += it.n_kv;
+      ++k;
     }
-    int prev_row = 0;  // this lane's page row of the previous key tile (its V is loaded one step later)
-    for (int t = 0; t <= n_kv; ++t) {
-      int row = a.pool_rows;  // out of range: the TMA fills zeros
-      bool have = false;
-      if (t < n_kv && lane < loads) {
-        const int pos = t * kPfKeys + lane * rpl;
-        if (pos < ctx_total) {
-          const int32_t blk = __ldg(trow + pos / B);
-          if (blk >= 0 && blk < a.num_blocks) {
-            have = true;
-            row = (blk * H + h) * B + pos % B;
-          } else {
-            atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
-          }
-        }
-      }
-      const uint32_t mask = __ballot_sync(0xffffffffu, have);
-      int ok = 1;
-      if (t < n_kv) {  // K of tile t
-        const int st = t % kKStages;
-        if (lane == 0) ok = mbar_wait(&bars.k_empty[st], ((t / kKStages) & 1) ^ 1, abort_flag, a.err_flag);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bars.k_full[st], kTileBytes);
-        for (int r = 0; r < loads; ++r) {
-          const int rr = __shfl_sync(0xffffffffu, row, r);
-          if (lane == 0) {
-            const uint32_t dst = base + kOffK + st * kTileBytes + (uint32_t)r * rpl * 128u;
-            tma_load_2d(dst, &tm_k, 0, rr, &bars.k_full[st]);
-            tma_load_2d(dst + kHalfBytes, &tm_k, 64, rr, &bars.k_full[st]);
-          }
-        }
-        ++k_issued;
-      }
-      if (t >= 1) {  // V of tile t - 1
-        const int tv = t - 1;
-        const int st = tv % kVStages;
-        if (lane == 0) ok = mbar_wait(&bars.v_empty[st], ((tv / kVStages) & 1) ^ 1, abort_flag, a.err_flag);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bars.v_full[st], kTileBytes);
-        for (int r = 0; r < loads; ++r) {
-          const int rr = __shfl_sync(0xffffffffu, prev_row, r);
-          if (lane == 0) {
-            const uint32_t dst = base + kOffV + st * kTileBytes + (uint32_t)r * rpl * 128u;
-            tma_load_2d(dst, &tm_v, 0, rr, &bars.v_full[st]);
-            tma_load_2d(dst + kHalfBytes, &tm_v, 64, rr, &bars.v_full[st]);
-          }
-        }
-        ++v_issued;
-      }
-      prev_row = row;
-    }
-    if (lane == 0 && *abort_flag) {  // let in-flight tiles land before exit
-      mbar_wait_drain(&bars.q_full, 0);
-      for (int t = max(0, k_issued - kKStages); t < k_issued; ++t)
-        mbar_wait_drain(&bars.k_full[t % kKStages], (t / kKStages) & 1);
-      for (int t = max(0, v_issued - kVStages); t < v_issued; ++t)
-        mbar_wait_drain(&bars.v_full[t % kVStages], (t / kVStages) & 1);
+    if (lane == 0 && *abort_flag) {  // let in-flight copies land before exit
+      if (k > 0) mbar_wait_drain(&bars.q_full, (k - 1) & 1);
+      for (int x = max(0, k_issued - kKStages); x < k_issued; ++x)
+        mbar_wait_drain(&bars.k_full[x % kKStages], (x / kKStages) & 1);
+      for (int x = max(0, v_issued - kVStages); x < v_issued; ++x)
+        mbar_wait_drain(&bars.v_full[x % kVStages], (x / kVStages) & 1);
     }
   } else if (warp == kPfMmaWarp) {
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
-      bool ok = mbar_wait(&bars.q_full, 0, abort_flag, a.err_flag);
       const uint64_t qdesc = smem_desc_sw128(base + kOffQ, 16, 1024);
-      // S(t) = Q K_t^T into score buffer t % 2
-      auto issue_s = [&](int t) -> bool {
-        if (!mbar_wait(&bars.k_full[t % kKStages], (t / kKStages) & 1, abort_flag, a.err_flag)) return false;
-        tc_fence_after();
-        // descriptors advance by adding (byte offset >> 4) to the start-address field
-        const uint64_t kdesc = smem_desc_sw128(base + kOffK + (t % kKStages) * kTileBytes, 16, 1024);
-        const uint32_t d = tmem + tmem_s(t & 1);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t koff = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-          umma_f16(d, qdesc + koff, kdesc + koff, a.idesc_s, kk > 0);
-        }
-        umma_commit(&bars.s_full[t & 1]);
-        umma_commit(&bars.k_empty[t % kKStages]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && n_kv > 1) ok = issue_s(1);
-      for (int t = 0; ok && t < n_kv; ++t) {
-        ok = mbar_wait(&bars.v_full[t % kVStages], (t / kVStages) & 1, abort_flag, a.err_flag);
-        if (ok && need_zero && t == n_kv - 1) ok = mbar_wait(&bars.v_zeroed, 0, abort_flag, a.err_flag);
-        const uint64_t vdesc = smem_desc_sw128(base + kOffV + (t % kVStages) * kTileBytes, kHalfBytes, 1024);
-        const uint32_t pb = tmem + tmem_s(t & 1);
-        const uint32_t first = t > 0 ? 1u : 0u;
-#pragma unroll
-        for (int hh = 0; hh < 2 && ok; ++hh) {  // O_h += P_h V_h: keys 64h .. 64h+63 of the tile
-          ok = mbar_wait(&bars.p_full[hh][t & 1], (t >> 1) & 1, abort_flag, a.err_flag);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {  // P_hi V, then P_lo V
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              umma_f16_ts(tmem + tmem_o(hh), pb + hh * 64 + part * 32 + kk * 8,
-                          vdesc + (((hh * 4 + kk) * 2048) >> 4), a.idesc_pv, (kk > 0 || part > 0) ? 1u : first);
-            }
-          }
-          umma_commit(&bars.pv_done[hh][t & 1]);
-        }
+      int g = 0, k = 0, nz = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const long long ipos = pf_round_pos(r);
+        if (ipos >= n_items) break;
+        PfItem it;
+        if (pf_item(a, order, npairs, (int)ipos, it) != kItemRun) continue;
+        const int n_kv = it.n_kv;
+        ok = mbar_wait(&bars.q_full, k & 1, abort_flag, a.err_flag);
         if (!ok) break;
-        umma_commit(&bars.v_empty[t % kVStages]);
-        if (t + 2 < n_kv) ok = issue_s(t + 2);  // after P(t) V in issue order: its buffer is free then
+        // S(x) = Q K_x^T into score buffer x % 2; after the item's last one the query buffer is free
+        auto issue_s = [&](int t) -> bool {
+          const int x = g + t;
+          if (!mbar_wait(&bars.k_full[x % kKStages], (x / kKStages) & 1, abort_flag, a.err_flag)) return false;
+          tc_fence_after();
+          // descriptors advance by adding (byte offset >> 4) to the start-address field
+          const uint64_t kdesc = smem_desc_sw128(base + kOffK + (x % kKStages) * kTileBytes, 16, 1024);
+          const uint32_t d = tmem + tmem_s(x & 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            umma_f16(d, qdesc + koff, kdesc + koff, a.idesc_s, kk > 0);
+          }
+          umma_commit(&bars.s_full[x & 1]);
+          umma_commit(&bars.k_empty[x % kKStages]);
+          if (t == n_kv - 1) umma_commit(&bars.q_empty);
+          return true;
+        };
+        ok = issue_s(0);
+        if (ok && n_kv > 1) ok = issue_s(1);
+        for (int t = 0; ok && t < n_kv; ++t) {
+          const int x = g + t;
+          ok = mbar_wait(&bars.v_full[x % kVStages], (x / kVStages) & 1, abort_flag, a.err_flag);
+          if (ok && it.need_zero && t == n_kv - 1) ok = mbar_wait(&bars.v_zeroed, nz & 1, abort_flag, a.err_flag);
+          // the previous item's epilogue has read both output accumulators
+          if (ok && t == 0) ok = mbar_wait(&bars.o_free, (k & 1) ^ 1, abort_flag, a.err_flag);
+          const uint64_t vdesc = smem_desc_sw128(base + kOffV + (x % kVStages) * kTileBytes, kHalfBytes, 1024);
+          const uint32_t pb = tmem + tmem_s(x & 1);
+          const uint32_t first = t > 0 ? 1u : 0u;
+#pragma unroll
+          for (int hh = 0; hh < 2 && ok; ++hh) {  // O_h += P_h V_h: keys 64h .. 64h+63 of the tile
+            ok = mbar_wait(&bars.p_full[hh][x & 1], (x >> 1) & 1, abort_flag, a.err_flag);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {  // P_hi V, then P_lo V
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                umma_f16_ts(tmem + tmem_o(hh), pb + hh * 64 + part * 32 + kk * 8,
+                            vdesc + (((hh * 4 + kk) * 2048) >> 4), a.idesc_pv, (kk > 0 || part > 0) ? 1u : first);
+              }
+            }
+            umma_commit(&bars.pv_done[hh][x & 1]);
+          }
+          if (!ok) break;
+          umma_commit(&bars.v_empty[x % kVStages]);
+          if (t + 2 < n_kv) ok = issue_s(t + 2);  // after P(x) V in issue order: its buffer is free then
+        }
+        if (it.need_zero) ++nz;
+        g += n_kv;
+        ++k;
       }
       // every issued MMA has finished before tensor memory is released
       umma_commit(&bars.drain);
@@ -519,136 +604,152 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int quarter = warp & 3;      // TMEM lane quarter this warp may access
     const int half = warp >> 2;        // columns 64*half .. 64*half+63
     const int r = quarter * 32 + lane; // query row within the tile = TMEM lane
-    const int qrow = row0 + r;
-    const int pos = c0 + qrow;
-    const int tile_first_pos = c0 + row0;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t full_mask = (1u << (kPfKeys / a.rows_per_load)) - 1u;
     const int col0 = half * 64;
     const uint32_t s_half = lane_addr + col0;  // + score buffer: this half's 64 columns
     const uint32_t o_mine = lane_addr + tmem_o(half);
-    // Page pieces of a key tile whose table entry is usable: the loader
-    // zero-fills the others and they are masked here.  Each lane < pieces
-    // reads one table entry, one tile ahead so the load latency is hidden.
     const int rpl = a.rows_per_load;
     const int pieces = kPfKeys / rpl;
-    const int32_t* trow = a.block_tables + (size_t)c * a.max_blocks_per_seq;
-    auto piece_entry = [&](int t) -> int32_t {
-      const int p = t * kPfKeys + lane * rpl;
-      return (t < n_kv && lane < pieces && p < ctx_total) ? __ldg(trow + p / B) : -1;
-    };
-    int32_t entry_next = piece_entry(0);
-    float m_used = -INFINITY;
-    float l = 0.f;
+    int g = 0, k = 0;
     bool ok = true;
-    for (int t = 0; t < n_kv; ++t) {
-      const int sb = t & 1;
-      const uint32_t kmask = __ballot_sync(0xffffffffu, entry_next >= 0 && entry_next < a.num_blocks);
-      entry_next = piece_entry(t + 1);
-      ok = mbar_wait(&bars.s_full[sb], (t >> 1) & 1, abort_flag, a.err_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[64];
-      tmem_ld64(s_half + tmem_s(sb), s);
-
-      const int key0 = t * kPfKeys;
-      const bool interior = key0 + kPfKeys - 1 <= tile_first_pos && key0 + kPfKeys <= ctx_total && kmask == full_mask;
-      if (!interior) {
-        const int lim = min(pos, ctx_total - 1) - key0;  // last admissible column of this row
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const int col = col0 + i;
-          const bool valid = col <= lim && ((kmask >> (col >> a.rpl_shift)) & 1u);
-          s[i] = valid ? s[i] : -INFINITY;
-        }
-      }
-      float mx4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-      for (int i = 4; i < 64; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
-      const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.qscale;  // qscale > 0
-      const float m_new = fmaxf(m_used, rmax);
-      const bool resc = m_new > m_used + kRescaleThreshold;  // also true when m_used is -inf
-      const float m_next = resc ? m_new : m_used;
-      const float alpha = resc ? ((m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_next)) : 1.f;
-      l *= alpha;
-      const float mref = (m_next == -INFINITY) ? 0.f : m_next;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t hw[32], lw[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float p0 = ex2_approx(fmaf(s[2 * e], a.qscale, -mref));
-        const float p1 = ex2_approx(fmaf(s[2 * e + 1], a.qscale, -mref));
-        sum4[e & 3] += p0 + p1;
-        split2<T>(p0, p1, hw[e], lw[e]);
-      }
-      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      // This half's columns of the buffer still hold P_h(t-2): wait for
-      // P_h(t-2) V.  A rescale of O_h also needs P_h(t-1) V in it.
-      const bool any_resc = t > 0 && __any_sync(0xffffffffu, resc);
-      if (t >= 2) ok = mbar_wait(&bars.pv_done[half][t & 1], ((t - 2) >> 1) & 1, abort_flag, a.err_flag);
-      if (ok && any_resc)
-        ok = mbar_wait(&bars.pv_done[half][(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, a.err_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // P_h over this half's scores: P_hi in its first 32 words, P_lo in the next 32
-      const uint32_t pw = s_half + tmem_s(sb);
-      tmem_st16(pw, hw);
-      tmem_st16(pw + 16, hw + 16);
-      tmem_st16(pw + 32, lw);
-      tmem_st16(pw + 48, lw + 16);
-      if (any_resc) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
-          tmem_ld32(o_mine + cc * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(o_mine + cc * 32, o);
-        }
-      }
-      tmem_st_wait();
-      if (half == 0 && need_zero && t == n_kv - 1) {
-        // zero the V rows of this last key tile that lie past the context
-        ok = mbar_wait(&bars.v_full[t % kVStages], (t / kVStages) & 1, abort_flag, a.err_flag);
+    for (int rr = 0; ok; ++rr) {
+      const long long ipos = pf_round_pos(rr);
+      if (ipos >= n_items) break;
+      PfItem it;
+      if (pf_item(a, order, npairs, (int)ipos, it) != kItemRun) continue;
+      const int n_kv = it.n_kv;
+      const int qrow = it.row0 + r;
+      const int pos = it.c0 + qrow;
+      const int tile_first_pos = it.c0 + it.row0;
+      const int ctx_total = it.ctx_total;
+      // Page pieces of a key tile whose table entry is usable: the loader
+      // zero-fills the others and they are masked here.  Each lane < pieces
+      // reads one table entry, one tile ahead so the load latency is hidden.
+      const int32_t* trow = a.block_tables + (size_t)it.c * a.max_blocks_per_seq;
+      auto piece_entry = [&](int t) -> int32_t {
+        const int p = t * kPfKeys + lane * rpl;
+        return (t < n_kv && lane < pieces && p < ctx_total) ? __ldg(trow + p / B) : -1;
+      };
+      int32_t entry_next = piece_entry(0);
+      float m_used = -INFINITY;
+      float l = 0.f;
+      for (int t = 0; t < n_kv; ++t) {
+        const int x = g + t;
+        const int sb = x & 1;
+        const uint32_t kmask = __ballot_sync(0xffffffffu, entry_next >= 0 && entry_next < a.num_blocks);
+        entry_next = piece_entry(t + 1);
+        ok = mbar_wait(&bars.s_full[sb], (x >> 1) & 1, abort_flag, a.err_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        if (key0 + r >= ctx_total) {
-          uint8_t* vbuf = gbase + kOffV + (t % kVStages) * kTileBytes;
-          const uint4 z = make_uint4(0, 0, 0, 0);
+        tc_fence_after();
+        float s[64];
+        tmem_ld64(s_half + tmem_s(sb), s);
+
+        const int key0 = t * kPfKeys;
+        const bool interior =
+            key0 + kPfKeys - 1 <= tile_first_pos && key0 + kPfKeys <= ctx_total && kmask == full_mask;
+        if (!interior) {
+          const int lim = min(pos, ctx_total - 1) - key0;  // last admissible column of this row
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            *reinterpret_cast<uint4*>(vbuf + r * 128 + ch * 16) = z;
-            *reinterpret_cast<uint4*>(vbuf + kHalfBytes + r * 128 + ch * 16) = z;
+          for (int i = 0; i < 64; ++i) {
+            const int col = col0 + i;
+            const bool valid = col <= lim && ((kmask >> (col >> a.rpl_shift)) & 1u);
+            s[i] = valid ? s[i] : -INFINITY;
           }
         }
-        fence_proxy_async_smem();
+        float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int i = 4; i < 64; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+        const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.qscale;  // qscale > 0
+        const float m_new = fmaxf(m_used, rmax);
+        const bool resc = m_new > m_used + kRescaleThreshold;  // also true when m_used is -inf
+        const float m_next = resc ? m_new : m_used;
+        const float alpha = resc ? ((m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_next)) : 1.f;
+        l *= alpha;
+        const float mref = (m_next == -INFINITY) ? 0.f : m_next;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t hw[32], lw[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = ex2_approx(fmaf(s[2 * e], a.qscale, -mref));
+          const float p1 = ex2_approx(fmaf(s[2 * e + 1], a.qscale, -mref));
+          sum4[e & 3] += p0 + p1;
+          split2<T>(p0, p1, hw[e], lw[e]);
+        }
+        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        // This half's columns of the buffer held P_h(x-2): wait for P_h(x-2) V.
+        // A rescale of O_h also needs P_h(x-1) V (same item) in it.
+        const bool any_resc = t > 0 && __any_sync(0xffffffffu, resc);
+        if (x >= 2) ok = mbar_wait(&bars.pv_done[half][sb], ((x - 2) >> 1) & 1, abort_flag, a.err_flag);
+        if (ok && any_resc)
+          ok = mbar_wait(&bars.pv_done[half][(x - 1) & 1], ((x - 1) >> 1) & 1, abort_flag, a.err_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // P_h over this half's scores: P_hi in its first 32 words, P_lo in the next 32
+        const uint32_t pw = s_half + tmem_s(sb);
+        tmem_st16(pw, hw);
+        tmem_st16(pw + 16, hw + 16);
+        tmem_st16(pw + 32, lw);
+        tmem_st16(pw + 48, lw + 16);
+        if (any_resc) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            tmem_ld32(o_mine + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(o_mine + cc * 32, o);
+          }
+        }
+        tmem_st_wait();
+        if (half == 0 && it.need_zero && t == n_kv - 1) {
+          // zero the V rows of this last key tile that lie past the context
+          ok = mbar_wait(&bars.v_full[x % kVStages], (x / kVStages) & 1, abort_flag, a.err_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          if (key0 + r >= ctx_total) {
+            uint8_t* vbuf = gbase + kOffV + (x % kVStages) * kTileBytes;
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              *reinterpret_cast<uint4*>(vbuf + r * 128 + ch * 16) = z;
+              *reinterpret_cast<uint4*>(vbuf + kHalfBytes + r * 128 + ch * 16) = z;
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.v_zeroed);
+        }
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.v_zeroed);
+        if (lane == 0) mbar_arrive(&bars.p_full[half][sb]);
+        m_used = m_next;
       }
-      tc_fence_before();
+      if (!ok) break;
+      // ---- epilogue: merge the two half-rows (log-sum-exp), write this half's 64 output columns
+      const int xl_ = g + n_kv - 1;  // the item's last key tile
+      ok = mbar_wait(&bars.pv_done[half][xl_ & 1], (xl_ >> 1) & 1, abort_flag, a.err_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      bars.xm[half][r] = m_used;
+      bars.xl[half][r] = l;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full[half][sb]);
-      m_used = m_next;
-    }
-    // ---- epilogue: merge the two half-rows (log-sum-exp), write this half's 64 output columns
-    if (ok) ok = mbar_wait(&bars.pv_done[half][(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, abort_flag, a.err_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    bars.xm[half][r] = m_used;
-    bars.xl[half][r] = l;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars.xbar[quarter]);
-    if (ok) ok = mbar_wait(&bars.xbar[quarter], 0, abort_flag, a.err_flag);
-    // the partner's output must be complete too before its columns are read
-    if (ok) ok = mbar_wait(&bars.pv_done[1 - half][(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, abort_flag, a.err_flag);
-    if (__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) mbar_arrive(&bars.xbar[quarter]);
+      ok = mbar_wait(&bars.xbar[quarter], k & 1, abort_flag, a.err_flag);
+      // the partner's output must be complete too before its columns are read
+      if (ok) ok = mbar_wait(&bars.pv_done[1 - half][xl_ & 1], (xl_ >> 1) & 1, abort_flag, a.err_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const float m0 = bars.xm[0][r], m1 = bars.xm[1][r];
       const float M = fmaxf(m0, m1);
@@ -657,8 +758,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float lt = w0 * bars.xl[0][r] + w1 * bars.xl[1][r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float c0w = w0 * inv, c1w = w1 * inv;
-      const bool store = qrow < n_c;
-      const size_t obase = ((size_t)(q0 + qrow) * H + h) * kPfD + col0;
+      const bool store = qrow < it.n_c;
+      const size_t obase = ((size_t)(it.q0 + qrow) * H + it.h) * kPfD + col0;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         float oa[32], ob[32];
@@ -694,6 +795,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
+      // this warp is done with both accumulators and with xm / xl of this item
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.o_free);
+      g += n_kv;
+      ++k;
     }
   }
   tc_fence_before();
@@ -817,9 +924,12 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
   }
   a.num_chunks = num_chunks;
   a.qtiles = (max_q_len + pa::kPfRows - 1) / pa::kPfRows;
-  const long long nblocks = (long long)a.qtiles * num_chunks * num_heads;
-  if (nblocks >= (1ll << 31)) return PA_ERR_INVALID_ARG;
-  dim3 grid((unsigned)nblocks);
+  const long long n_items = (long long)a.qtiles * num_chunks * num_heads;
+  if (n_items >= (1ll << 31)) return PA_ERR_INVALID_ARG;
+  const int sms = pa_host::device_sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+  // persistent: one CTA per SM (shared memory and tensor memory allow one)
+  dim3 grid((unsigned)(n_items < sms ? n_items : sms));
   kern<<<grid, pa::kPfThreads, pa::kPfSmemBytes, (cudaStream_t)stream>>>(tm_q, tm_k, tm_v, a);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -115,3 +115,29 @@ def test_prefill_flags_bad_table_entry(pa):
     out, flags, _, _ = run_prefill(pa, m, "f32", tables=bad)
     assert flags == pa.PA_FLAG_BAD_BLOCK
     assert torch.isfinite(out).all()
+
+
+def test_prefill_many_items_per_cta(pa):
+    """Ten or so (query tile, head) items per CTA of the persistent grid, with
+    an empty chunk and chunks of one row among them: every item's output must
+    come out right whatever ran on the same CTA before it."""
+    m = W.small_prefill(chunk_lens=(700, 0, 300, 513, 129, 1, 255), ctx_before=(40, 77, 0, 1500, 129, 2047, 333),
+                        H=16, B=16)
+    out, flags, _, _ = run_prefill(pa, m, "f32")
+    assert flags == 0
+    ref, _, _ = oracle_prefill(m)
+    assert_attn_close(out, ref, "f32", "prefill many items")
+
+
+@pytest.mark.parametrize("n_chunks", [1000, 1100])
+def test_prefill_many_short_chunks(pa, n_chunks):
+    """More (chunk, query tile) pairs than the in-kernel ranking handles
+    (1100) and just under it (1000): both work orders give the same result."""
+    g = torch.Generator().manual_seed(5)
+    cl = tuple(int(x) for x in torch.randint(1, 4, (n_chunks,), generator=g))
+    cb = tuple(int(x) for x in torch.randint(0, 200, (n_chunks,), generator=g))
+    m = W.small_prefill(chunk_lens=cl, ctx_before=cb, H=2, B=16)
+    out, flags, _, _ = run_prefill(pa, m, "bf16")
+    assert flags == 0
+    ref, _, _ = oracle_prefill(m)
+    assert_attn_close(out, ref, "bf16", f"prefill {n_chunks} short chunks")

@@ -209,6 +209,36 @@ int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_
                      int dtype, int32_t* err_flag, void* stream);
 
 /*
+ * pa_mixed_step -- one step of a mixed batch: decode of num_seqs sequences
+ * and prefill of num_chunks chunks over the same pools, run concurrently.
+ * [cb] "Chunked prefill" and its scheduler: a step's token budget holds the
+ * running requests' decode tokens and prefill chunks together and runs them
+ * as one forward pass.
+ *  - dec_* and the decode arguments are those of pa_decode (partition size
+ *    chosen automatically); pf_* and the chunk arguments those of
+ *    pa_prefill_chunk; pools, num_heads, head_dim, block_size, num_blocks,
+ *    scale, dtype and err_flag are shared.  head_dim must be 128 (prefill).
+ *  - The prefill runs on `aux_stream` on at most `prefill_sms` SMs
+ *    (<= 0: PA_MIXED_PREFILL_SHARE percent of them), launched first; the
+ *    decode runs on `stream` on the rest of the GPU.  aux_stream first waits
+ *    for the work queued on `stream` before the call; `stream` then waits for
+ *    the prefill, so work queued on `stream` after the call sees both outputs.
+ *    aux_stream must be a stream other than `stream` (NULL is rejected).
+ *  - Outputs: the same values as pa_decode and pa_prefill_chunk give.
+ *  - All arguments of both parts are checked before anything is launched.
+ *    Events are created and destroyed per call; nothing is allocated on the
+ *    device.
+ */
+#define PA_MIXED_PREFILL_SHARE 45
+int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int32_t* dec_block_tables,
+                  int dec_max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+                  void* workspace, size_t workspace_bytes, void* pf_out, int pf_out_dtype, const void* pf_q,
+                  const int32_t* cu_q_lens, const int32_t* ctx_before, const int32_t* pf_block_tables,
+                  int pf_max_blocks_per_seq, int num_chunks, int total_q, int max_q_len, const void* k_pool,
+                  const void* v_pool, int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                  int dtype, int prefill_sms, int32_t* err_flag, void* stream, void* aux_stream);
+
+/*
  * pa_get_error -- synchronise `stream`, read the device error flag, clear it.
  * Returns PA_OK, PA_ERR_TIMEOUT (if PA_FLAG_TIMEOUT is set), PA_ERR_BAD_INDEX
  * (any other flag) or PA_ERR_CUDA.  If flags_out is non-null it receives the

@@ -258,6 +258,15 @@ def mixed_prefill(device="cpu", num_decode=32, chunk_len=512, ctx_before=(1024, 
     )
 
 
+def budget512_step(device="cpu") -> MixedWorkload:
+    """One step under a 512-token budget, filled the way the continuous
+    batching page's scheduler fills it: the 32 running requests' decode tokens
+    first (contexts uniform in [256, 4096]), then 480 tokens of the prefill in
+    progress -- the fourth 480-token chunk of a long prompt, at context 1440.
+    40 heads x 128, page size 256, bf16."""
+    return mixed_prefill(device=device, num_decode=32, chunk_len=480, ctx_before=(1440,))
+
+
 def small_prefill(device="cpu", chunk_lens=(130, 77), ctx_before=(200, 37), H=3, D=128, B=16,
                   dtype="bf16", seed=SEED_DATA) -> MixedWorkload:
     """A small chunked-prefill case (ragged chunks, ragged contexts) that the

@@ -53,6 +53,8 @@ SIGNATURES = {
     "pa_decode": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _I, _P, _P], _I),
     "pa_decode_static_scratch": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P], _I),
     "pa_prefill_chunk": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P], _I),
+    "pa_mixed_step": ([_P, _I, _P, _P, _I, _P, _I, _I, _P, _Z, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I,
+                       _I, _I, _F, _I, _I, _P, _P, _P], _I),
     "pa_get_error": ([_P, _P, _P], _I),
     "pa_slot_mapping": ([_P, _I, _I, _I, _P, _P, _I, _P], _I),
     "pa_alloc_create": ([_I, _I, _P], _I),
@@ -235,6 +237,38 @@ def pa_prefill_chunk(out, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables
         _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1], C, T, int(max_q_len), H, D, B, NB,
         float(scale), _kv_code(k_pool), _dev(err_flag, "err_flag", torch.int32), _stream(stream))
     _check(st, "pa_prefill_chunk")
+
+
+def pa_mixed_step(dec_out, dec_q, dec_block_tables, context_lens, max_context_len, workspace, pf_out, pf_q,
+                  cu_q_lens, ctx_before, pf_block_tables, max_q_len, k_pool, v_pool, scale, err_flag, aux_stream,
+                  prefill_sms=0, stream=None):
+    """Decode of dec_q [S][H][D] and prefill of the chunks in pf_q [total][H][D]
+    over the same pools, concurrently: the prefill on aux_stream (a
+    torch.cuda.Stream other than `stream`), the decode on `stream`."""
+    NB, H, B, D = k_pool.shape
+    S = dec_q.shape[0]
+    T = pf_q.shape[0]
+    C = ctx_before.shape[0]
+    if tuple(dec_q.shape) != (S, H, D) or tuple(dec_out.shape) != (S, H, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("decode shape mismatch")
+    if dec_block_tables.dim() != 2 or dec_block_tables.shape[0] < S or context_lens.shape != (S,):
+        raise ValueError("dec_block_tables must be [>=S][MB], context_lens [S]")
+    if tuple(pf_q.shape) != (T, H, D) or tuple(pf_out.shape) != (T, H, D) or cu_q_lens.shape != (C + 1,):
+        raise ValueError("prefill shape mismatch")
+    if pf_block_tables.dim() != 2 or pf_block_tables.shape[0] < C:
+        raise ValueError("pf_block_tables must be [>=C][MB]")
+    st = lib().pa_mixed_step(
+        _dev(dec_out, "dec_out", (torch.float16, torch.bfloat16, torch.float32)), _TORCH_TO_PA[dec_out.dtype],
+        _dev(dec_q, "dec_q", k_pool.dtype), _dev(dec_block_tables, "dec_block_tables", torch.int32),
+        dec_block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(pf_out, "pf_out", (torch.float16, torch.bfloat16, torch.float32)), _TORCH_TO_PA[pf_out.dtype],
+        _dev(pf_q, "pf_q", k_pool.dtype), _dev(cu_q_lens, "cu_q_lens", torch.int32),
+        _dev(ctx_before, "ctx_before", torch.int32), _dev(pf_block_tables, "pf_block_tables", torch.int32),
+        pf_block_tables.shape[1], C, T, int(max_q_len), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        H, D, B, NB, float(scale), _kv_code(k_pool), int(prefill_sms), _dev(err_flag, "err_flag", torch.int32),
+        _stream(stream), _stream(aux_stream))
+    _check(st, "pa_mixed_step")
 
 
 def pa_get_error(err_flag, stream=None) -> int:

@@ -166,4 +166,21 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 int device_sm_count();
 
+// Argument checks of pa_decode / pa_prefill_chunk that launch nothing, and
+// the prefill launch with its persistent grid capped at max_ctas CTAs
+// (0 = one per SM).  Defined next to the kernels.
+int decode_check(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
+                 const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                 int max_context_len, int num_seqs, int num_heads, int head_dim, int block_size, int num_blocks,
+                 float scale, int dtype, void* workspace, size_t workspace_bytes, int partition_size,
+                 int32_t* err_flag);
+int prefill_check(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_before,
+                  const void* k_pool, const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                  int num_chunks, int total_q, int max_q_len, int num_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, int dtype, int32_t* err_flag);
+int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_before,
+                   const void* k_pool, const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                   int num_chunks, int total_q, int max_q_len, int num_heads, int head_dim, int block_size,
+                   int num_blocks, float scale, int dtype, int32_t* err_flag, int max_ctas, void* stream);
+
 }  // namespace pa_host

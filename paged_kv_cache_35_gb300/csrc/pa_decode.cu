@@ -630,7 +630,78 @@ int launch_decode(const pa::DecodeArgs& a, cudaStream_t stream) {
   return PA_OK;
 }
 
+// Checks pa_decode's arguments and fills the kernel arguments; launches
+// nothing.  *empty is set when there is no work (num_seqs == 0).
+int decode_setup(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
+                 const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                 int max_context_len, int num_seqs, int num_heads, int head_dim, int block_size, int num_blocks,
+                 float scale, int dtype, void* workspace, size_t workspace_bytes, int partition_size,
+                 int32_t* err_flag, pa::DecodeArgs& a, bool& empty) {
+  empty = false;
+  if (!pa_host::is_kv_dtype(dtype) || !pa_host::is_out_dtype(out_dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size <= 0 || block_size % pa::kChunk != 0 || block_size > 65536) return PA_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) {
+    empty = true;
+    return PA_OK;
+  }
+  if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens || !workspace || !err_flag)
+    return PA_ERR_INVALID_ARG;
+  if (!pa_host::aligned16(q) || !pa_host::aligned16(k_pool) || !pa_host::aligned16(v_pool) ||
+      !pa_host::aligned16(workspace) || !pa_host::aligned16(out))
+    return PA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if ((long long)num_seqs * num_heads > (1ll << 30)) return PA_ERR_INVALID_ARG;
+  const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
+  if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return PA_ERR_INVALID_ARG;
+  const int max_parts = decode_max_parts(max_context_len, P);
+  const WsLayout w = ws_layout(num_seqs, num_heads, head_dim, max_parts);
+  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.max_context_len = max_context_len;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.qscale = scale * 1.4426950408889634f;
+  a.partition_size = P;
+  a.max_parts = max_parts;
+  char* ws = static_cast<char*>(workspace);
+  a.counters = reinterpret_cast<int*>(ws + w.counters);
+  a.items = reinterpret_cast<int4*>(ws + w.items);
+  a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
+  a.part_o = reinterpret_cast<float*>(ws + w.o);
+  a.err_flag = err_flag;
+  return PA_OK;
+}
+
 }  // namespace
+
+namespace pa_host {
+
+int decode_check(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
+                 const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                 int max_context_len, int num_seqs, int num_heads, int head_dim, int block_size, int num_blocks,
+                 float scale, int dtype, void* workspace, size_t workspace_bytes, int partition_size,
+                 int32_t* err_flag) {
+  pa::DecodeArgs a;
+  bool empty = false;
+  return decode_setup(out, out_dtype, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                      max_context_len, num_seqs, num_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
+                      workspace_bytes, partition_size, err_flag, a, empty);
+}
+
+}  // namespace pa_host
 
 extern "C" {
 
@@ -654,48 +725,12 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
               int num_seqs, int num_heads, int head_dim, int block_size, int num_blocks, float scale, int dtype,
               void* workspace, size_t workspace_bytes, int partition_size, int32_t* err_flag, void* stream) {
-  if (!pa_host::is_kv_dtype(dtype) || !pa_host::is_out_dtype(out_dtype)) return PA_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size <= 0 || block_size % pa::kChunk != 0 || block_size > 65536) return PA_ERR_UNSUPPORTED;
-  if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
-    return PA_ERR_INVALID_ARG;
-  if (num_seqs == 0) return PA_OK;
-  if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens || !workspace || !err_flag)
-    return PA_ERR_INVALID_ARG;
-  if (!pa_host::aligned16(q) || !pa_host::aligned16(k_pool) || !pa_host::aligned16(v_pool) ||
-      !pa_host::aligned16(workspace) || !pa_host::aligned16(out))
-    return PA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID_ARG;
-  if ((long long)num_seqs * num_heads > (1ll << 30)) return PA_ERR_INVALID_ARG;
-  const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
-  if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return PA_ERR_INVALID_ARG;
-  const int max_parts = decode_max_parts(max_context_len, P);
-  const WsLayout w = ws_layout(num_seqs, num_heads, head_dim, max_parts);
-  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
-
   pa::DecodeArgs a;
-  a.out = out;
-  a.out_dtype = out_dtype;
-  a.q = q;
-  a.k_pool = k_pool;
-  a.v_pool = v_pool;
-  a.block_tables = block_tables;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.context_lens = context_lens;
-  a.max_context_len = max_context_len;
-  a.num_seqs = num_seqs;
-  a.num_heads = num_heads;
-  a.block_size = block_size;
-  a.num_blocks = num_blocks;
-  a.qscale = scale * 1.4426950408889634f;
-  a.partition_size = P;
-  a.max_parts = max_parts;
-  char* ws = static_cast<char*>(workspace);
-  a.counters = reinterpret_cast<int*>(ws + w.counters);
-  a.items = reinterpret_cast<int4*>(ws + w.items);
-  a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
-  a.part_o = reinterpret_cast<float*>(ws + w.o);
-  a.err_flag = err_flag;
+  bool empty = false;
+  const int st = decode_setup(out, out_dtype, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                              max_context_len, num_seqs, num_heads, head_dim, block_size, num_blocks, scale, dtype,
+                              workspace, workspace_bytes, partition_size, err_flag, a, empty);
+  if (st != PA_OK || empty) return st;
   cudaStream_t s = (cudaStream_t)stream;
   if (head_dim == 128) {
     return dtype == PA_F16 ? launch_decode<128, __half>(a, s) : launch_decode<128, __nv_bfloat16>(a, s);

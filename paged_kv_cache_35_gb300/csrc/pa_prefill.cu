@@ -843,20 +843,24 @@ uint32_t make_idesc(uint32_t ab_format, bool b_mn_major) {
   return d;
 }
 
-}  // namespace
-
-extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens,
-                                const int32_t* ctx_before, const void* k_pool, const void* v_pool,
-                                const int32_t* block_tables, int max_blocks_per_seq, int num_chunks, int total_q,
-                                int max_q_len, int num_heads, int head_dim, int block_size, int num_blocks,
-                                float scale, int dtype, int32_t* err_flag, void* stream) {
+// Checks pa_prefill_chunk's arguments, encodes the tensor maps and fills the
+// kernel arguments; launches nothing.  *empty is set when there is no work.
+int prefill_setup(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_before,
+                  const void* k_pool, const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                  int num_chunks, int total_q, int max_q_len, int num_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, int dtype, int32_t* err_flag, pa::PrefillArgs& a, CUtensorMap& tm_q,
+                  CUtensorMap& tm_k, CUtensorMap& tm_v, bool& empty) {
+  empty = false;
   if (!pa_host::is_kv_dtype(dtype) || !pa_host::is_out_dtype(out_dtype)) return PA_ERR_UNSUPPORTED;
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (block_size <= 0 || block_size % 16 != 0 || !(128 % block_size == 0 || block_size % 128 == 0))
     return PA_ERR_UNSUPPORTED;
   if (num_chunks < 0 || total_q < 0 || max_q_len < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
     return PA_ERR_INVALID_ARG;
-  if (num_chunks == 0 || total_q == 0 || max_q_len == 0) return PA_OK;
+  if (num_chunks == 0 || total_q == 0 || max_q_len == 0) {
+    empty = true;
+    return PA_OK;
+  }
   if (num_heads > 65535) return PA_ERR_INVALID_ARG;
   if (!out || !q || !cu_q_lens || !ctx_before || !k_pool || !v_pool || !block_tables || !err_flag)
     return PA_ERR_INVALID_ARG;
@@ -866,11 +870,12 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
   if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID_ARG;
   const uint64_t pool_rows = (uint64_t)num_blocks * num_heads * block_size;
   if (pool_rows >= (1ull << 31)) return PA_ERR_INVALID_ARG;
+  const long long qtiles = (max_q_len + pa::kPfRows - 1) / pa::kPfRows;
+  if (qtiles * num_chunks * num_heads >= (1ll << 31)) return PA_ERR_INVALID_ARG;
 
   auto encode = get_encode_fn();
   if (encode == nullptr) return PA_ERR_CUDA;
   const CUtensorMapDataType tdt = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap tm_q, tm_k, tm_v;
   {
     cuuint64_t dims[3] = {128, (cuuint64_t)num_heads, (cuuint64_t)total_q};
     cuuint64_t strides[2] = {128 * 2, (cuuint64_t)num_heads * 128 * 2};
@@ -893,7 +898,6 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
       return PA_ERR_CUDA;
   }
 
-  pa::PrefillArgs a;
   a.out = out;
   a.out_dtype = out_dtype;
   a.cu_q_lens = cu_q_lens;
@@ -911,8 +915,41 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
   a.idesc_s = make_idesc(fmt, false);
   a.idesc_pv = make_idesc(fmt, true);
   a.err_flag = err_flag;
+  a.num_chunks = num_chunks;
+  a.qtiles = (int)qtiles;
+  return PA_OK;
+}
+
+}  // namespace
+
+namespace pa_host {
+
+int prefill_check(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_before,
+                  const void* k_pool, const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                  int num_chunks, int total_q, int max_q_len, int num_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, int dtype, int32_t* err_flag) {
+  pa::PrefillArgs a;
+  CUtensorMap tm_q, tm_k, tm_v;
+  bool empty = false;
+  return prefill_setup(out, out_dtype, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                       num_chunks, total_q, max_q_len, num_heads, head_dim, block_size, num_blocks, scale, dtype,
+                       err_flag, a, tm_q, tm_k, tm_v, empty);
+}
+
+int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_before,
+                   const void* k_pool, const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                   int num_chunks, int total_q, int max_q_len, int num_heads, int head_dim, int block_size,
+                   int num_blocks, float scale, int dtype, int32_t* err_flag, int max_ctas, void* stream) {
+  pa::PrefillArgs a;
+  CUtensorMap tm_q, tm_k, tm_v;
+  bool empty = false;
+  const int st = prefill_setup(out, out_dtype, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables,
+                               max_blocks_per_seq, num_chunks, total_q, max_q_len, num_heads, head_dim, block_size,
+                               num_blocks, scale, dtype, err_flag, a, tm_q, tm_k, tm_v, empty);
+  if (st != PA_OK || empty) return st;
 
   auto kern = dtype == PA_BF16 ? pa::prefill_kernel<__nv_bfloat16> : pa::prefill_kernel<__half>;
+  const int fmt = dtype == PA_BF16 ? 1 : 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
   static int configured[2][64] = {{0}};
@@ -922,14 +959,24 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
       return PA_ERR_CUDA;
     configured[fmt][dev] = 1;
   }
-  a.num_chunks = num_chunks;
-  a.qtiles = (max_q_len + pa::kPfRows - 1) / pa::kPfRows;
   const long long n_items = (long long)a.qtiles * num_chunks * num_heads;
-  if (n_items >= (1ll << 31)) return PA_ERR_INVALID_ARG;
-  const int sms = pa_host::device_sm_count();
+  const int sms = device_sm_count();
   if (sms <= 0) return PA_ERR_CUDA;
-  // persistent: one CTA per SM (shared memory and tensor memory allow one)
-  dim3 grid((unsigned)(n_items < sms ? n_items : sms));
-  kern<<<grid, pa::kPfThreads, pa::kPfSmemBytes, (cudaStream_t)stream>>>(tm_q, tm_k, tm_v, a);
+  // persistent: at most one CTA per SM (shared and tensor memory allow one)
+  long long ctas = max_ctas > 0 && max_ctas < sms ? max_ctas : sms;
+  if (ctas > n_items) ctas = n_items;
+  kern<<<dim3((unsigned)ctas), pa::kPfThreads, pa::kPfSmemBytes, (cudaStream_t)stream>>>(tm_q, tm_k, tm_v, a);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa_host
+
+extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens,
+                                const int32_t* ctx_before, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, int max_blocks_per_seq, int num_chunks, int total_q,
+                                int max_q_len, int num_heads, int head_dim, int block_size, int num_blocks,
+                                float scale, int dtype, int32_t* err_flag, void* stream) {
+  return pa_host::prefill_launch(out, out_dtype, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables,
+                                 max_blocks_per_seq, num_chunks, total_q, max_q_len, num_heads, head_dim, block_size,
+                                 num_blocks, scale, dtype, err_flag, 0, stream);
 }

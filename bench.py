@@ -193,7 +193,10 @@ WORKLOAD_TEXT = {
                      "40 heads x 128, block 16, fp16, copy-on-write through the host allocator",
     "mixed": "mixed_chunked_prefill: 32 decode seqs (ctx U[256,4096]) + 2 chunks x 512 queries at ctx 1024/3072, "
              "40 heads x 128, page 256, bf16",
+    "budget512": "budget512_step: 512-token budget = 32 decode seqs (ctx U[256,4096]) + one 480-query chunk at "
+                 "ctx 1440, 40 heads x 128, page 256, bf16",
 }
+MIXED = ("mixed", "budget512")
 
 
 def workload_config(name, w):
@@ -201,9 +204,10 @@ def workload_config(name, w):
             "head_dim": w.head_dim, "block_size": w.block_size, "pool_blocks": w.num_blocks, "kv_dtype": w.dtype,
             "placement": "seeded random permutation of the pool" if name != "shared_prefix" else
             "host allocator (free list from the end, copy-on-write)",
-            "step": "pa_reshape_and_cache (1 new token/seq) + pa_decode over ctx" +
-                    (" + pa_prefill_chunk (2 x 512 queries, their K/V in the same scatter)" if name == "mixed" else ""),
-            "l2": "no flush: K/V read per step >> 129 MB L2" if name in ("llama13b", "long_context", "mixed") else
+            "step": ("pa_reshape_and_cache (decode tokens + chunk tokens) + pa_mixed_step (decode on the caller's "
+                     "stream and chunked prefill on a second stream, concurrently)" if name in MIXED else
+                     "pa_reshape_and_cache (1 new token/seq) + pa_decode over ctx"),
+            "l2": "no flush: K/V read per step >> 129 MB L2" if name in ("llama13b", "long_context") + MIXED else
                   "working set partly L2-resident (reported as such)"}
 
 
@@ -366,7 +370,7 @@ def run_ours(args, rank, world, local):
     elif name == "shared_prefix":
         w = shared_prefix_decode_workload(pa, W, dev)
     else:
-        mixed = W.mixed_prefill(device=dev)
+        mixed = W.mixed_prefill(device=dev) if name == "mixed" else W.budget512_step(device=dev)
         w = mixed.decode
     S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
     elt = 2
@@ -393,15 +397,27 @@ def run_ours(args, rank, world, local):
     ws = pa.decode_workspace(S, H, D, mx, device=dev)
     err = pa.new_error_flag(dev)
     stream = torch.cuda.current_stream(dev)
+    aux = torch.cuda.Stream(dev, priority=-1) if mixed is not None else None  # see pa_mixed_step in pa.h
 
     def prefill():
         pa.pa_prefill_chunk(pout, mixed.chunk_q, cu_d, cb_d, w.k_pool, w.v_pool, ctab_d, mq, w.scale, err, stream)
 
+    def decode(q_in=None):
+        pa.pa_decode(out, w.q if q_in is None else q_in, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err,
+                     stream=stream)
+
+    def mixed_step(q_in=None, tables_in=None, ctx_in=None, cq_in=None, cu_in=None, cb_in=None, ctab_in=None):
+        pick = lambda given, resident: resident if given is None else given
+        pa.pa_mixed_step(out, pick(q_in, w.q), pick(tables_in, tables_d), pick(ctx_in, ctx_d), mx, ws, pout,
+                         pick(cq_in, mixed.chunk_q), pick(cu_in, cu_d), pick(cb_in, cb_d), pick(ctab_in, ctab_d), mq,
+                         w.k_pool, w.v_pool, w.scale, err, aux, stream=stream)
+
     def step():
         pa.pa_reshape_and_cache(k_new, v_new, w.k_pool, w.v_pool, slots_d, err, stream)
-        pa.pa_decode(out, w.q, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err, stream=stream)
         if mixed is not None:
-            prefill()
+            mixed_step()
+        else:
+            decode()
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -420,11 +436,37 @@ def run_ours(args, rank, world, local):
                      for c0, n in zip(mixed.ctx_before.tolist(), mixed.chunk_lens.tolist()))
     step_b = dbytes + sbytes + pbytes
 
-    # ---- device-timed region
     K = args.steps
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    dec_s, dec_e = [ev() for _ in range(K)], [ev() for _ in range(K)]
-    pre_s, pre_e = ([ev() for _ in range(K)], [ev() for _ in range(K)]) if mixed is not None else ([], [])
+    seq_ms = None
+    if mixed is not None:
+        # Component pass (untimed for the headline): each kernel alone, per-call
+        # events, for the rooflines -- inside the concurrent step the decode's
+        # events would also span the wait for the prefill -- and the two parts
+        # one after the other, for comparison with the concurrent step.
+        Kc = min(K, 200)
+        dec_s, dec_e = [ev() for _ in range(Kc)], [ev() for _ in range(Kc)]
+        pre_s, pre_e = [ev() for _ in range(Kc)], [ev() for _ in range(Kc)]
+        c0_, c1_ = ev(), ev()
+        torch.cuda.synchronize(dev)
+        c0_.record(stream)
+        for i in range(Kc):
+            pa.pa_reshape_and_cache(k_new, v_new, w.k_pool, w.v_pool, slots_d, err, stream)
+            dec_s[i].record(stream)
+            decode()
+            dec_e[i].record(stream)
+            pre_s[i].record(stream)
+            prefill()
+            pre_e[i].record(stream)
+        c1_.record(stream)
+        torch.cuda.synchronize(dev)
+        dec_ms = [a.elapsed_time(b) for a, b in zip(dec_s, dec_e)]
+        pre_ms = [a.elapsed_time(b) for a, b in zip(pre_s, pre_e)]
+        seq_ms = c0_.elapsed_time(c1_) / Kc
+
+    # ---- device-timed region
+    if mixed is None:
+        dec_s, dec_e = [ev() for _ in range(K)], [ev() for _ in range(K)]
     t_start, t_end = ev(), ev()
     clocks = ClockSampler(local)
     clocks.start()
@@ -435,21 +477,20 @@ def run_ours(args, rank, world, local):
     t_start.record(stream)
     for i in range(K):
         pa.pa_reshape_and_cache(k_new, v_new, w.k_pool, w.v_pool, slots_d, err, stream)
-        dec_s[i].record(stream)
-        pa.pa_decode(out, w.q, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err, stream=stream)
-        dec_e[i].record(stream)
         if mixed is not None:
-            pre_s[i].record(stream)
-            prefill()
-            pre_e[i].record(stream)
+            mixed_step()
+        else:
+            dec_s[i].record(stream)
+            decode()
+            dec_e[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     h1 = time.time()
     dist_barrier(world)
     clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    dec_ms = [a.elapsed_time(b) for a, b in zip(dec_s, dec_e)]
-    pre_ms = [a.elapsed_time(b) for a, b in zip(pre_s, pre_e)]
+    if mixed is None:
+        dec_ms = [a.elapsed_time(b) for a, b in zip(dec_s, dec_e)]
     flags = pa.pa_get_error(err, stream)
     if flags:
         raise RuntimeError(f"device error flags {flags} in the timed region")
@@ -470,8 +511,10 @@ def run_ours(args, rank, world, local):
     outs = [(h_out, out)]
     if mixed is not None:
         h_cq, h_pout = pin(mixed.chunk_q), torch.empty(T, H, D, dtype=tdt).pin_memory()
-        d_cq = torch.empty_like(mixed.chunk_q)
-        pairs.append((d_cq, h_cq))
+        h_cu, h_cb, h_ctab = pin(cu_d), pin(cb_d), pin(ctab_d)
+        d_cq, d_cu, d_cb, d_ctab = (torch.empty_like(mixed.chunk_q), torch.empty_like(cu_d), torch.empty_like(cb_d),
+                                    torch.empty_like(ctab_d))
+        pairs += [(d_cq, h_cq), (d_cu, h_cu), (d_cb, h_cb), (d_ctab, h_ctab)]
         outs.append((h_pout, pout))
     h2d = sum(h.numel() * h.element_size() for _, h in pairs)
     d2h = sum(h.numel() * h.element_size() for h, _ in outs)
@@ -480,9 +523,10 @@ def run_ours(args, rank, world, local):
         for d, h in pairs:
             d.copy_(h, non_blocking=True)
         pa.pa_reshape_and_cache(d_k, d_v, w.k_pool, w.v_pool, d_slots, err, stream)
-        pa.pa_decode(out, d_q, w.k_pool, w.v_pool, d_tables, d_ctx, mx, w.scale, ws, err, stream=stream)
         if mixed is not None:
-            pa.pa_prefill_chunk(pout, d_cq, cu_d, cb_d, w.k_pool, w.v_pool, ctab_d, mq, w.scale, err, stream)
+            mixed_step(d_q, d_tables, d_ctx, d_cq, d_cu, d_cb, d_ctab)
+        else:
+            pa.pa_decode(out, d_q, w.k_pool, w.v_pool, d_tables, d_ctx, mx, w.scale, ws, err, stream=stream)
         for h, d in outs:
             h.copy_(d, non_blocking=True)
 
@@ -529,6 +573,10 @@ def run_ours(args, rank, world, local):
         line["roofline"]["note"] = ("logical bytes: shared prompt blocks are counted once per sample that reads "
                                     "them; the unique K/V footprint is config.unique_kv_bytes")
     if mixed is not None:
+        line["roofline"]["note"] = ("decode kernel timed alone in a component pass before the timed region (inside "
+                                    "the concurrent step its events would also span the prefill)")
+        line["sequential_ms_per_step"] = seq_ms
+        line["concurrent_speedup_vs_sequential"] = seq_ms / (max_ms / K)
         bf16_peak = load_tensor_peak()
         pre_avg_s = statistics.mean(pre_ms) / 1e3
         line["prefill"] = {"bound": "tensor", "achieved": pflops / pre_avg_s / 1e12, "unit": "TFLOP/s",

@@ -224,6 +224,12 @@ int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_
  *    for the work queued on `stream` before the call; `stream` then waits for
  *    the prefill, so work queued on `stream` after the call sees both outputs.
  *    aux_stream must be a stream other than `stream` (NULL is rejected).
+ *    Give aux_stream a higher priority than `stream`
+ *    (cudaStreamCreateWithPriority): when steps are queued back to back both
+ *    parts become ready at the same moment, and the priority makes the block
+ *    scheduler place the prefill's CTAs first; otherwise the decode's grid
+ *    may fill every SM and the two parts run one after the other (correct,
+ *    but without the overlap).
  *  - Outputs: the same values as pa_decode and pa_prefill_chunk give.
  *  - All arguments of both parts are checked before anything is launched.
  *    Events are created and destroyed per call; nothing is allocated on the

@@ -244,7 +244,8 @@ def pa_mixed_step(dec_out, dec_q, dec_block_tables, context_lens, max_context_le
                   prefill_sms=0, stream=None):
     """Decode of dec_q [S][H][D] and prefill of the chunks in pf_q [total][H][D]
     over the same pools, concurrently: the prefill on aux_stream (a
-    torch.cuda.Stream other than `stream`), the decode on `stream`."""
+    torch.cuda.Stream other than `stream`, created with a higher priority,
+    e.g. torch.cuda.Stream(priority=-1)), the decode on `stream`."""
     NB, H, B, D = k_pool.shape
     S = dec_q.shape[0]
     T = pf_q.shape[0]

@@ -85,7 +85,7 @@ def test_mixed_step_is_bit_identical_to_separate_calls(pa):
     pa.pa_reshape_and_cache(st.k_new, st.v_new, w.k_pool, w.v_pool, st.slots, err)
     ref_d, ref_p = st.separate(pa, err)
     assert pa.pa_get_error(err) == 0
-    aux = torch.cuda.Stream()
+    aux = torch.cuda.Stream(priority=-1)
     for sms in (0, 1, 24, 76, 10000):  # auto share, one SM, a few, half, more than the GPU has
         d, p = st.mixed(pa, err, aux, prefill_sms=sms)
         assert pa.pa_get_error(err) == 0
@@ -103,7 +103,7 @@ def test_mixed_step_budget512_matches_oracle(pa):
     chunk_k, chunk_v, chunk_q = m.chunk_k.cpu(), m.chunk_v.cpu(), m.chunk_q.cpu()
     st = Step(pa, m)
     err = pa.new_error_flag()
-    main, aux = torch.cuda.Stream(), torch.cuda.Stream()
+    main, aux = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
     torch.cuda.synchronize()
     with torch.cuda.stream(main):
         pa.pa_reshape_and_cache(st.k_new, st.v_new, w.k_pool, w.v_pool, st.slots, err, stream=main)

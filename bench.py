@@ -197,6 +197,8 @@ WORKLOAD_TEXT = {
                  "ctx 1440, 40 heads x 128, page 256, bf16",
 }
 MIXED = ("mixed", "budget512")
+WORKLOAD_TEXT["swap"] = ("block swap: K/V of 8 requests x 2048 tokens, 40 heads x 128, fp16, block sizes 16..256, "
+                         "GPU pool (blocks scattered) <-> pinned host pool")
 
 
 def workload_config(name, w):
@@ -598,6 +600,81 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_swap(args, rank, world, local):
+    """Block swap between the GPU pool and a pinned host pool, by block size:
+    the swap side of the pages' swap-versus-recompute comparison.  Each
+    replica swaps the K/V of 8 requests x 2048 tokens (40 heads x 128, fp16)
+    out to the host pool and back in, through pa_swap_blocks with the blocks
+    scattered over a pool twice that size; the link's ceiling is one
+    contiguous copy of the same bytes, timed the same way in the same run."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_35_gb300 as pa
+    import pa_workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    H, D, tokens = 40, 128, 8 * 2048
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    K = max(1, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(max(3, min(args.warmup, 10))):
+            fn()
+        torch.cuda.synchronize(dev)
+        dist_barrier(world)
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return dist_max(a.elapsed_time(b) / K, world)
+
+    sweep = []
+    err = pa.new_error_flag(dev)
+    for B in (16, 32, 64, 128, 256):
+        nb = tokens // B
+        gk = W.normal((2 * nb, H, B, D), 71, torch.float16, dev)
+        gv = W.normal((2 * nb, H, B, D), 72, torch.float16, dev)
+        ck = torch.empty(nb, H, B, D, dtype=torch.float16).pin_memory()
+        cv = torch.empty_like(ck).pin_memory()
+        g = torch.Generator().manual_seed(B)
+        scattered = torch.randperm(2 * nb, generator=g)[:nb]
+        out_pairs = torch.stack([scattered, torch.arange(nb)], 1).to(torch.int32).to(dev)
+        in_pairs = torch.stack([torch.arange(nb), scattered.flip(0)], 1).to(torch.int32).to(dev)
+        nbytes = 2 * nb * H * B * D * 2
+        t_out = timed(lambda: pa.pa_swap_blocks(gk, gv, ck, cv, out_pairs, err, stream))
+        t_in = timed(lambda: pa.pa_swap_blocks(ck, cv, gk, gv, in_pairs, err, stream))
+        slab_k, slab_v = gk[:nb], gv[:nb]
+        t_cout = timed(lambda: (ck.copy_(slab_k, non_blocking=True), cv.copy_(slab_v, non_blocking=True)))
+        t_cin = timed(lambda: (slab_k.copy_(ck, non_blocking=True), slab_v.copy_(cv, non_blocking=True)))
+        if pa.pa_get_error(err, stream):
+            raise RuntimeError("device error flags during the swap sweep")
+        sweep.append({"block_size": B, "blocks": nb, "bytes": nbytes,
+                      "swap_out_ms": t_out, "swap_in_ms": t_in,
+                      "swap_out_GBs": nbytes / t_out / 1e6, "swap_in_GBs": nbytes / t_in / 1e6,
+                      "contiguous_out_GBs": nbytes / t_cout / 1e6, "contiguous_in_GBs": nbytes / t_cin / 1e6})
+        del gk, gv, ck, cv
+    head = sweep[0]
+    value = 2 * head["bytes"] * world / ((head["swap_out_ms"] + head["swap_in_ms"]) / 1e3) / 1e9
+    link = 2 * head["bytes"] / ((head["bytes"] / head["contiguous_out_GBs"] + head["bytes"] / head["contiguous_in_GBs"])
+                                / 1e9) / 1e9
+    line = {"metric": "paged KV block swap, GPU pool <-> pinned host pool (swap-out + swap-in)", "value": value,
+            "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": max(3, min(args.warmup, 10)),
+            "ms_per_step": head["swap_out_ms"] + head["swap_in_ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT["swap"], "block_size": 16, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "link", "achieved": value / world, "peak": link, "unit": "GB/s",
+                         "frac": value / world / link, "traffic": None,
+                         "peak_kind": "measured in this run: one contiguous copy of the same bytes each way"},
+            "gpu_launches": 2 * K, "sweep_by_block_size": sweep}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -614,7 +691,10 @@ def main():
         run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
         return
     rank, world, local = dist_setup()
-    run_ours(args, rank, world, local)
+    if args.workload == "swap":
+        run_swap(args, rank, world, local)
+    else:
+        run_ours(args, rank, world, local)
     if world > 1:
         import torch.distributed as dist
 

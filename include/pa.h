@@ -107,6 +107,37 @@ int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int n_pairs
                    int head_dim, int block_size, int num_blocks, int dtype, int32_t* err_flag, void* stream);
 
 /*
+ * pa_swap_blocks -- move whole blocks between two pools, one of which may be
+ * a pinned host pool: swap-out of a preempted request's blocks to CPU memory
+ * and swap-in when it resumes.
+ * [summary] section 5: under memory pressure the preemptive scheduler swaps
+ * some sequences' KV blocks to CPU memory (or recomputes them), and Figure 26
+ * compares the two by block size; [cb] "오프로딩" (offloading): the request's
+ * KV blocks are copied into a pre-allocated pinned CPU buffer, every request
+ * that fits the swap pool in one batched transfer, and copied back to the GPU
+ * when space frees up.
+ *   for i in [0, n_pairs): (s, d) = (pairs[2i], pairs[2i+1]):
+ *     dst_K[d][:][:][:] = src_K[s][:][:][:], same for V (all heads, all slots).
+ * src_k, src_v: the source pool [src_num_blocks][num_heads][block_size][head_dim];
+ * dst_k, dst_v: the destination pool [dst_num_blocks][...], same shape per block
+ * and dtype.  Each pool is either device memory or pinned host memory that
+ * the GPU can address (cudaHostAlloc / cudaMallocHost, or cudaHostRegister
+ * with cudaHostRegisterMapped; with unified addressing the host address is
+ * the device address).  The copy is one kernel launch for the whole batch:
+ * the GPU reads and writes the host pool directly over the CPU-GPU link, so
+ * neither the block size nor the scattering of the block ids adds a per-copy
+ * cost.  Bit-exact.
+ * pairs: device int32 [n_pairs][2], n_pairs <= 65535.  Destinations must be
+ * distinct and, when both pools are the same memory, disjoint from the
+ * sources.  An id outside its pool sets PA_FLAG_BAD_BLOCK and that pair is
+ * skipped.  n_pairs == 0 is a no-op.  The host pool must stay pinned until
+ * the stream has passed the call.
+ */
+int pa_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks, void* dst_k, void* dst_v,
+                   int dst_num_blocks, const int32_t* pairs, int n_pairs, int num_heads, int head_dim,
+                   int block_size, int dtype, int32_t* err_flag, void* stream);
+
+/*
  * Split-KV partition length (tokens) that pa_decode uses when called with
  * partition_size == 0: a multiple of 16 between 64 and 1024, chosen from the
  * batch shape alone (no device query).

@@ -7,7 +7,8 @@ nothing from them.
 
 Contents:
   * ``pa_oracle.c``     -- plain fp64 C: reassembly + attention (decode and
-                           causal chunked prefill), slot scatter, block copy.
+                           causal chunked prefill), slot scatter, block copy,
+                           block swap between two pools.
                            Built into ``liboracle.so`` by ``build()``.
   * ``reference_np.py`` -- an independent numpy restatement of the same
                            definitions, plus the split-KV combine identity.
@@ -55,6 +56,7 @@ def lib():
         L.oracle_prefill.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, ctypes.c_double, i]
         L.oracle_reshape_and_cache.argtypes = [P, P, P, P, P, i, i, i, i, i]
         L.oracle_copy_blocks.argtypes = [P, P, P, i, i, i, i, i]
+        L.oracle_swap_blocks.argtypes = [P, P, i, P, P, i, P, i, i, i, i]
         L.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         L.oracle_f16_to_double.restype = ctypes.c_double
         L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -132,6 +134,19 @@ def copy_blocks(k_bits: np.ndarray, v_bits: np.ndarray, pairs, block_size):
     NB, H, B, D = k_bits.shape
     rc = lib().oracle_copy_blocks(_ptr(k_bits), _ptr(v_bits), _ptr(pr), pr.shape[0], H, D, B, NB)
     _check(rc, "copy_blocks")
+
+
+def swap_blocks(src_k: np.ndarray, src_v: np.ndarray, dst_k: np.ndarray, dst_v: np.ndarray, pairs) -> int:
+    """dst block d := src block s for each (s, d) in pairs (uint16 pool bits,
+    [blocks][H][B][D]); pairs with an id outside its pool are skipped.
+    Returns the number of skipped pairs."""
+    pr = _i32(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    NBs, H, B, D = src_k.shape
+    for a in (src_k, src_v, dst_k, dst_v):
+        if a.dtype != np.uint16 or not a.flags["C_CONTIGUOUS"] or tuple(a.shape[1:]) != (H, B, D):
+            raise ValueError("pools must be C-contiguous uint16 [blocks][H][B][D]")
+    return int(lib().oracle_swap_blocks(_ptr(src_k), _ptr(src_v), NBs, _ptr(dst_k), _ptr(dst_v), dst_k.shape[0],
+                                        _ptr(pr), pr.shape[0], H, D, B))
 
 
 def slot_of(table_row, pos: int, block_size: int) -> int:

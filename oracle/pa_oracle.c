@@ -273,6 +273,29 @@ int oracle_reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new, uint1
  * Copy-on-write block copy: for each pair (src, dst) in order, every slot of
  * every head of block src is copied bitwise into block dst, in K and in V.
  */
+/* Block swap between two pools ([summary] section 5: a preempted sequence's
+ * KV blocks are swapped out to CPU memory and back in; [cb] "오프로딩": the
+ * blocks are copied into a pinned CPU buffer and copied back on resume).
+ * For each pair (s, d): dst block d := src block s, K and V, every head and
+ * slot.  A pair with an id outside its pool is skipped; the return value is
+ * the number of skipped pairs. */
+int oracle_swap_blocks(const uint16_t* src_k, const uint16_t* src_v, int src_num_blocks, uint16_t* dst_k,
+                       uint16_t* dst_v, int dst_num_blocks, const int32_t* pairs, int num_pairs, int num_heads,
+                       int head_dim, int block_size) {
+  const int64_t per_block = (int64_t)num_heads * block_size * head_dim;
+  int skipped = 0;
+  for (int i = 0; i < num_pairs; ++i) {
+    const int32_t s = pairs[2 * i], d = pairs[2 * i + 1];
+    if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks) {
+      ++skipped;
+      continue;
+    }
+    memcpy(dst_k + d * per_block, src_k + s * per_block, sizeof(uint16_t) * per_block);
+    memcpy(dst_v + d * per_block, src_v + s * per_block, sizeof(uint16_t) * per_block);
+  }
+  return skipped;
+}
+
 int oracle_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32_t* pairs, int num_pairs,
                        int num_heads, int head_dim, int block_size, int num_blocks) {
   const int64_t per_block = (int64_t)num_heads * block_size * head_dim;

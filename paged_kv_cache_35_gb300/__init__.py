@@ -55,6 +55,7 @@ SIGNATURES = {
     "pa_prefill_chunk": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P], _I),
     "pa_mixed_step": ([_P, _I, _P, _P, _I, _P, _I, _I, _P, _Z, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I,
                        _I, _I, _F, _I, _I, _P, _P, _P], _I),
+    "pa_swap_blocks": ([_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pa_get_error": ([_P, _P, _P], _I),
     "pa_slot_mapping": ([_P, _I, _I, _I, _P, _P, _I, _P], _I),
     "pa_alloc_create": ([_I, _I, _P], _I),
@@ -164,6 +165,39 @@ def pa_copy_blocks(k_pool, v_pool, pairs, err_flag, stream=None):
         _dev(pairs, "pairs", torch.int32) if n else None, n, H, D, B, NB, _kv_code(k_pool),
         _dev(err_flag, "err_flag", torch.int32), _stream(stream))
     _check(st, "pa_copy_blocks")
+
+
+def _pool_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
+    """Address of a pool that lives on the GPU or in pinned host memory."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
+    if t.is_cuda:
+        return _dev(t, name, dtype)
+    if not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return t.data_ptr()
+
+
+def pa_swap_blocks(src_k, src_v, dst_k, dst_v, pairs, err_flag, stream=None):
+    """Copy whole blocks from pool src to pool dst: pairs int32 [n][2] of
+    (src block, dst block) on the GPU.  Either pool may be a pinned host
+    tensor ([blocks][H][B][D], same per-block shape and dtype)."""
+    NBs, H, B, D = src_k.shape
+    NBd = dst_k.shape[0]
+    if src_v.shape != src_k.shape or dst_v.shape != dst_k.shape or tuple(dst_k.shape[1:]) != (H, B, D):
+        raise ValueError("pool shape mismatch")
+    n = pairs.shape[0] if pairs.numel() else 0
+    if n and tuple(pairs.shape) != (n, 2):
+        raise ValueError("pairs must be [n][2]")
+    st = lib().pa_swap_blocks(
+        _pool_ptr(src_k, "src_k"), _pool_ptr(src_v, "src_v", src_k.dtype), NBs, _pool_ptr(dst_k, "dst_k", src_k.dtype),
+        _pool_ptr(dst_v, "dst_v", src_k.dtype), NBd, _dev(pairs, "pairs", torch.int32) if n else None, n, H, D, B,
+        _kv_code(src_k), _dev(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "pa_swap_blocks")
 
 
 def pa_decode_partition_size(num_seqs: int, num_heads: int, max_context_len: int) -> int:

@@ -1,8 +1,10 @@
-// KV write (slot scatter), copy-on-write block copy, and the error-flag and
-// status entry points of the C ABI.
+// KV write (slot scatter), copy-on-write block copy, block swap between a
+// GPU pool and a pinned host pool, and the error-flag and status entry points
+// of the C ABI.
 //
-// Both kernels are pure byte movers bound by HBM bandwidth: 16-byte vector
-// loads and stores, grid-stride loops sized to a multiple of the SM count.
+// The kernels are pure byte movers: 16-byte vector loads and stores,
+// grid-stride loops.  The scatter and the block copy are bound by HBM
+// bandwidth, the swap by the CPU-GPU link.
 #include <cstdio>
 
 #include "pa_common.cuh"
@@ -56,6 +58,50 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_
   uint4* vd = v_pool + (int64_t)dst * vecs_per_block;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < vecs_per_block;
        i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 a = ks[i];
+    const uint4 b = vs[i];
+    kd[i] = a;
+    vd[i] = b;
+  }
+}
+
+// Whole-block moves between two pools, either of which may be pinned host
+// memory read or written through its device address (swap-out / swap-in).
+// grid.y = pair; each CTA walks a strided share of the block's K and V
+// vectors with four vectors of each in flight per thread, since a load from
+// the host side of the link takes several times an HBM load's latency.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const uint4* __restrict__ src_k,
+                                                          const uint4* __restrict__ src_v, int src_num_blocks,
+                                                          uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                                                          int dst_num_blocks, const int32_t* __restrict__ pairs,
+                                                          int64_t vecs_per_block, int32_t* err_flag) {
+  const int pair = blockIdx.y;
+  const int32_t src = __ldg(pairs + 2 * pair);
+  const int32_t dst = __ldg(pairs + 2 * pair + 1);
+  if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err_flag, PA_FLAG_BAD_BLOCK);
+    return;
+  }
+  const uint4* ks = src_k + (int64_t)src * vecs_per_block;
+  const uint4* vs = src_v + (int64_t)src * vecs_per_block;
+  uint4* kd = dst_k + (int64_t)dst * vecs_per_block;
+  uint4* vd = dst_v + (int64_t)dst * vecs_per_block;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < vecs_per_block; i += 4 * stride) {
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a[u] = ks[i + u * stride];
+      b[u] = vs[i + u * stride];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      kd[i + u * stride] = a[u];
+      vd[i + u * stride] = b[u];
+    }
+  }
+  for (; i < vecs_per_block; i += stride) {
     const uint4 a = ks[i];
     const uint4 b = vs[i];
     kd[i] = a;
@@ -141,6 +187,31 @@ int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int n_pairs
   dim3 grid((unsigned)per_pair, (unsigned)n_pairs);
   pa::copy_blocks_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>((uint4*)k_pool, (uint4*)v_pool, pairs,
                                                                      vecs_per_block, num_blocks, err_flag);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks, void* dst_k, void* dst_v,
+                   int dst_num_blocks, const int32_t* pairs, int n_pairs, int num_heads, int head_dim,
+                   int block_size, int dtype, int32_t* err_flag, void* stream) {
+  if (n_pairs < 0 || num_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!pa_host::is_kv_dtype(dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim <= 0 || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  if (n_pairs == 0) return PA_OK;
+  if (n_pairs > 65535) return PA_ERR_INVALID_ARG;
+  if (!src_k || !src_v || !dst_k || !dst_v || !pairs || !err_flag) return PA_ERR_INVALID_ARG;
+  if (!pa_host::aligned16(src_k) || !pa_host::aligned16(src_v) || !pa_host::aligned16(dst_k) ||
+      !pa_host::aligned16(dst_v))
+    return PA_ERR_INVALID_ARG;
+  const int64_t vecs_per_block = (int64_t)num_heads * block_size * head_dim / 8;
+  const int threads = 256;
+  int64_t per_pair = (vecs_per_block + 4 * threads - 1) / (4 * threads);
+  if (per_pair > 64) per_pair = 64;
+  if (per_pair < 1) per_pair = 1;
+  dim3 grid((unsigned)per_pair, (unsigned)n_pairs);
+  pa::swap_blocks_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(
+      (const uint4*)src_k, (const uint4*)src_v, src_num_blocks, (uint4*)dst_k, (uint4*)dst_v, dst_num_blocks, pairs,
+      vecs_per_block, err_flag);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

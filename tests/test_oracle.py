@@ -321,6 +321,28 @@ def test_copy_blocks_is_whole_block_bitwise():
         oracle.copy_blocks(kb, vb, [(0, NB)], B)
 
 
+def test_swap_blocks_moves_whole_blocks_between_pools():
+    """Swap-out to a second (host) pool and swap-in to other blocks: each
+    block is filled with its own id, so where every block's contents went is
+    checked by value, including the pools' untouched blocks and a skipped
+    pair with an id outside its pool."""
+    NB_gpu, NB_cpu, H, B, D = 6, 4, 2, 16, 8
+    ids = lambda n, off: np.repeat(np.arange(off, off + n, dtype=np.uint16), H * B * D).reshape(n, H, B, D)
+    gk, gv = ids(NB_gpu, 0), ids(NB_gpu, 100)
+    ck, cv = ids(NB_cpu, 50), ids(NB_cpu, 150)
+    skipped = oracle.swap_blocks(gk, gv, ck, cv, [(4, 0), (1, 3), (2, NB_cpu)])  # out: gpu 4 -> cpu 0, 1 -> 3
+    assert skipped == 1
+    assert [int(ck[b, 0, 0, 0]) for b in range(NB_cpu)] == [4, 51, 52, 1]
+    assert [int(cv[b, 1, 15, 7]) for b in range(NB_cpu)] == [104, 151, 152, 101]
+    assert (gk == ids(NB_gpu, 0)).all() and (gv == ids(NB_gpu, 100)).all()  # the source is left as it was
+    skipped = oracle.swap_blocks(ck, cv, gk, gv, [(0, 5), (3, 2), (-1, 0)])  # in: cpu 0 -> gpu 5, cpu 3 -> gpu 2
+    assert skipped == 1
+    assert [int(gk[b, 1, 3, 2]) for b in range(NB_gpu)] == [0, 1, 1, 3, 4, 4]
+    assert [int(gv[b, 0, 0, 0]) for b in range(NB_gpu)] == [100, 101, 101, 103, 104, 104]
+    for pool in (gk, gv, ck, cv):  # whole blocks: every element of a block holds one value
+        assert (pool == pool[:, :1, :1, :1]).all()
+
+
 # -- planted mistakes: the pins must catch them --------------------------------
 
 def _paged_vs_contiguous_error(decode_fn):

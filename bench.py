@@ -586,6 +586,8 @@ def run_ours(args, rank, world, local):
                            "peak_kind": bf16_peak[1], "algorithmic_flops_per_launch": pflops,
                            "avg_launch_ms": pre_avg_s * 1e3,
                            "tensor_flops_executed_per_launch": pflops * 3 // 2}
+    if name == "tiny":
+        line["graph_replay"] = graph_replay_comparison(pa, w, dev, stream)
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
 
@@ -598,6 +600,58 @@ def run_ours(args, rank, world, local):
                                           f"{t_rep * reps:.1f} s wall"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def graph_replay_comparison(pa, w, dev, stream, n=2000):
+    """The decode step issued as a direct pa_decode call and as a replay of
+    its recorded CUDA graph (DecodeGraphs, sequence interval 8, KV interval
+    256): steps back to back (host issue cost and device time per step) and
+    one step alone (launch to completion)."""
+    import torch
+
+    S, H, D = w.num_seqs, w.num_heads, w.head_dim
+    mx = int(w.context_lens.max())
+    tables, ctx = w.block_tables.to(dev), w.context_lens.to(dev)
+    out = torch.empty(S, H, D, dtype=w.q.dtype, device=dev)
+    err = pa.new_error_flag(dev)
+    ws = pa.decode_workspace(S, H, D, mx, device=dev)
+    g = pa.DecodeGraphs(w.k_pool, w.v_pool, max_seqs=S, max_context_len=mx, max_blocks_per_seq=w.max_blocks_per_seq,
+                        scale=w.scale, err_flag=err, seq_interval=8, kv_interval=256)
+    g.q[:S] = w.q
+    g.tables[:S, :w.max_blocks_per_seq] = tables
+    g.context_lens[:S] = ctx
+    fns = {"direct": lambda: pa.pa_decode(out, w.q, w.k_pool, w.v_pool, tables, ctx, mx, w.scale, ws, err,
+                                          stream=stream),
+           "graph": lambda: g.run(S, mx, stream)}
+    res = {}
+    for label, fn in fns.items():
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        t1 = time.perf_counter()
+        torch.cuda.synchronize(dev)
+        one = []
+        for _ in range(50):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            one.append(a.elapsed_time(b) * 1e3)
+        res[label] = {"us_per_step_back_to_back": e0.elapsed_time(e1) / n * 1e3,
+                      "host_us_per_call": (t1 - t0) / n * 1e6, "us_one_step_alone": statistics.median(one)}
+    if pa.pa_get_error(err, stream):
+        raise RuntimeError("device error flags in the graph replay comparison")
+    res["graphs_recorded"] = g.count
+    g.close()
+    return res
 
 
 def run_swap(args, rank, world, local):

@@ -276,6 +276,48 @@ int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int
                   int dtype, int prefill_sms, int32_t* err_flag, void* stream, void* aux_stream);
 
 /*
+ * Decode graphs -- pa_decode recorded once per padded batch shape and
+ * replayed.  [cb] "CUDA 그래프": a step's CPU work (batch assembly, kernel
+ * dispatch) is removed by recording the GPU work once and replaying it for
+ * batches of the same shape; because the shape changes every step, the query
+ * count and the KV length are padded up to multiples of fixed intervals, the
+ * recorded graphs are cached by padded shape, and a new shape triggers a new
+ * recording.
+ *
+ * The graphs read and write caller-owned STATIC device buffers given at
+ * creation, sized for the largest padded batch:
+ *   q_buf, out_buf  [S_max][num_heads][head_dim]   (q in dtype, out in out_dtype)
+ *   tables_buf      int32 [S_max][max_blocks_per_seq]
+ *   ctx_buf         int32 [S_max]
+ *   workspace       pa_decode_graphs_workspace_bytes(...) bytes, 16-byte aligned
+ * with S_max = max_seqs rounded up to seq_interval.  The pools, scale, dtype
+ * and err_flag are fixed at creation too.  Per step the caller writes rows
+ * 0 .. num_seqs-1 of q_buf, tables_buf and ctx_buf (on the stream it passes
+ * to _run, or before), then calls _run(num_seqs, max_context_len): the
+ * shape is padded to (num_seqs up to a multiple of seq_interval,
+ * max_context_len up to a multiple of kv_interval), ctx_buf rows num_seqs ..
+ * padded-1 are zeroed on the stream (zero output rows), and the graph of that
+ * padded shape is replayed on the stream -- recorded first, on a stream of the
+ * object's own, if the shape is new.  Rows 0 .. num_seqs-1 of out_buf then
+ * hold what pa_decode(..., num_seqs = padded, max_context_len = padded)
+ * gives.  Shapes beyond the creation maxima: PA_ERR_INVALID_ARG.
+ * The object holds host state only (no device memory); it is not thread-safe
+ * and must be used on the device that was current at creation.
+ */
+typedef struct pa_decode_graphs pa_decode_graphs;
+size_t pa_decode_graphs_workspace_bytes(int max_seqs, int num_heads, int head_dim, int max_context_len,
+                                        int seq_interval, int kv_interval);
+int pa_decode_graphs_create(void* out_buf, int out_dtype, const void* q_buf, const void* k_pool,
+                            const void* v_pool, const int32_t* tables_buf, int max_blocks_per_seq,
+                            int32_t* ctx_buf, int max_seqs, int max_context_len, int num_heads, int head_dim,
+                            int block_size, int num_blocks, float scale, int dtype, void* workspace,
+                            size_t workspace_bytes, int seq_interval, int kv_interval, int32_t* err_flag,
+                            pa_decode_graphs** out);
+int pa_decode_graphs_run(pa_decode_graphs* g, int num_seqs, int max_context_len, void* stream);
+int pa_decode_graphs_count(const pa_decode_graphs* g); /* graphs recorded so far */
+void pa_decode_graphs_destroy(pa_decode_graphs* g);
+
+/*
  * pa_get_error -- synchronise `stream`, read the device error flag, clear it.
  * Returns PA_OK, PA_ERR_TIMEOUT (if PA_FLAG_TIMEOUT is set), PA_ERR_BAD_INDEX
  * (any other flag) or PA_ERR_CUDA.  If flags_out is non-null it receives the

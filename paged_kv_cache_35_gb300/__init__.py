@@ -56,6 +56,12 @@ SIGNATURES = {
     "pa_mixed_step": ([_P, _I, _P, _P, _I, _P, _I, _I, _P, _Z, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I,
                        _I, _I, _F, _I, _I, _P, _P, _P], _I),
     "pa_swap_blocks": ([_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pa_decode_graphs_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _Z),
+    "pa_decode_graphs_create": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _I, _I, _P,
+                                 _P], _I),
+    "pa_decode_graphs_run": ([_P, _I, _I, _P], _I),
+    "pa_decode_graphs_count": ([_P], _I),
+    "pa_decode_graphs_destroy": ([_P], None),
     "pa_get_error": ([_P, _P, _P], _I),
     "pa_slot_mapping": ([_P, _I, _I, _I, _P, _P, _I, _P], _I),
     "pa_alloc_create": ([_I, _I, _P], _I),
@@ -333,6 +339,55 @@ def pa_slot_mapping(block_tables, seq_idx, pos, block_size: int) -> np.ndarray:
                                si.shape[0], out.ctypes.data)
     _check(st, "pa_slot_mapping")
     return out
+
+
+class DecodeGraphs:
+    """pa_decode recorded once per padded (sequence count, KV length) shape
+    and replayed (see pa.h).  Owns the static device buffers the graphs use:
+    write the step's rows into .q, .tables and .context_lens, then run()."""
+
+    def __init__(self, k_pool, v_pool, max_seqs, max_context_len, max_blocks_per_seq, scale, err_flag,
+                 seq_interval=8, kv_interval=256, out_dtype=None):
+        NB, H, B, D = k_pool.shape
+        dev = k_pool.device
+        s_max = -(-max_seqs // seq_interval) * seq_interval
+        self.k_pool, self.v_pool, self.err_flag = k_pool, v_pool, err_flag
+        self.q = torch.zeros(s_max, H, D, dtype=k_pool.dtype, device=dev)
+        self.out = torch.zeros(s_max, H, D, dtype=out_dtype or k_pool.dtype, device=dev)
+        self.tables = torch.full((s_max, max_blocks_per_seq), -1, dtype=torch.int32, device=dev)
+        self.context_lens = torch.zeros(s_max, dtype=torch.int32, device=dev)
+        n = int(lib().pa_decode_graphs_workspace_bytes(max_seqs, H, D, max_context_len, seq_interval, kv_interval))
+        if n == 0:
+            raise ValueError("bad sizes for decode graphs")
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+        h = ctypes.c_void_p()
+        st = lib().pa_decode_graphs_create(
+            _dev(self.out, "out"), _TORCH_TO_PA[self.out.dtype], _dev(self.q, "q"), _dev(k_pool, "k_pool"),
+            _dev(v_pool, "v_pool", k_pool.dtype), _dev(self.tables, "tables"), max_blocks_per_seq,
+            _dev(self.context_lens, "context_lens"), max_seqs, max_context_len, H, D, B, NB, float(scale),
+            _kv_code(k_pool), _dev(self.workspace, "workspace"), n, seq_interval, kv_interval,
+            _dev(err_flag, "err_flag", torch.int32), ctypes.byref(h))
+        _check(st, "pa_decode_graphs_create")
+        self._h = h
+
+    def run(self, num_seqs: int, max_context_len: int, stream=None):
+        _check(lib().pa_decode_graphs_run(self._h, int(num_seqs), int(max_context_len), _stream(stream)),
+               "pa_decode_graphs_run")
+
+    @property
+    def count(self) -> int:
+        return int(lib().pa_decode_graphs_count(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pa_decode_graphs_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class BlockAllocator:

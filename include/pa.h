@@ -355,6 +355,38 @@ typedef struct pa_alloc pa_alloc;
 
 int pa_alloc_create(int num_blocks, int block_size, pa_alloc** out);
 void pa_alloc_destroy(pa_alloc* a);
+
+/*
+ * Prefix caching ([cb] "Prefix 캐싱" and "제거" (eviction)): requests whose
+ * prompts share a prefix share the blocks that hold it.
+ *  - PA_ALLOC_PREFIX_CACHE in pa_alloc_create_ex's flags turns it on (without
+ *    it the calls below behave like add_seq / append_slots and reuse nothing).
+ *  - A sequence created by pa_alloc_add_seq_prefix and extended only through
+ *    pa_alloc_append_tokens has known token ids.  Each of its blocks that
+ *    becomes full is keyed by its whole prefix (the ids from position 0 to the
+ *    block's end) unless that prefix already has a block.
+ *  - pa_alloc_add_seq_prefix(tokens[0..n)) walks the prompt's full blocks from
+ *    the first: while the block's prefix has a cached block, that block joins
+ *    the new sequence (+1 reference).  *n_reused_tokens = the tokens covered
+ *    (a multiple of B): their K/V are already in the pool, so the prefill
+ *    starts after them; the remaining prompt tokens are appended with
+ *    pa_alloc_append_tokens.
+ *  - A block whose last reference goes keeps its content and key
+ *    ("initialized") and still matches.  When a block must be taken and no
+ *    block without content is free, the most recently freed initialized block
+ *    loses its key and is taken.  pa_alloc_num_free counts both kinds.
+ *  - pa_alloc_append_slots on such a sequence (ids unknown) ends its caching.
+ *  - Keys are 128-bit chained fingerprints of the prefix ids; a match also
+ *    compares the block's own ids.
+ */
+#define PA_ALLOC_PREFIX_CACHE 1
+int pa_alloc_create_ex(int num_blocks, int block_size, int flags, pa_alloc** out);
+int pa_alloc_add_seq_prefix(pa_alloc* a, int seq_id, const int32_t* tokens, int n_tokens, int* n_reused_tokens);
+/* pa_alloc_append_slots with the appended tokens' ids (token_ids int32 [n]). */
+int pa_alloc_append_tokens(pa_alloc* a, const int* seq_ids, const int32_t* token_ids, int n, int64_t* slots_out,
+                           int32_t* copy_pairs_out, int* n_pairs_out);
+/* Blocks holding a cache entry, and how many of them are free (initialized). */
+int pa_alloc_prefix_stats(const pa_alloc* a, int* cached_blocks, int* initialized_free_blocks);
 /* New empty sequence.  PA_ERR_INVALID_ARG if seq_id exists or is negative. */
 int pa_alloc_add_seq(pa_alloc* a, int seq_id);
 /* child shares all of parent's blocks.  PA_ERR_INVALID_ARG if parent missing / child exists. */

@@ -32,6 +32,7 @@ PA_ERR_TIMEOUT = 7
 PA_ERR_WORKSPACE = 8
 
 PA_F16, PA_BF16, PA_F32 = 0, 1, 2
+PA_ALLOC_PREFIX_CACHE = 1
 
 PA_FLAG_BAD_BLOCK = 1
 PA_FLAG_BAD_SLOT = 2
@@ -75,6 +76,10 @@ SIGNATURES = {
     "pa_alloc_num_free": ([_P], _I),
     "pa_alloc_ref": ([_P, _I], _I),
     "pa_alloc_num_seqs": ([_P], _I),
+    "pa_alloc_create_ex": ([_I, _I, _I, _P], _I),
+    "pa_alloc_add_seq_prefix": ([_P, _I, _P, _I, _P], _I),
+    "pa_alloc_append_tokens": ([_P, _P, _P, _I, _P, _P, _P], _I),
+    "pa_alloc_prefix_stats": ([_P, _P, _P], _I),
 }
 
 
@@ -393,11 +398,12 @@ class DecodeGraphs:
 class BlockAllocator:
     """Host block manager (free list, reference counts, copy-on-write)."""
 
-    def __init__(self, num_blocks: int, block_size: int):
+    def __init__(self, num_blocks: int, block_size: int, prefix_cache: bool = False):
         self.block_size = block_size
         self.num_blocks = num_blocks
         h = ctypes.c_void_p()
-        _check(lib().pa_alloc_create(num_blocks, block_size, ctypes.byref(h)), "pa_alloc_create")
+        flags = PA_ALLOC_PREFIX_CACHE if prefix_cache else 0
+        _check(lib().pa_alloc_create_ex(num_blocks, block_size, flags, ctypes.byref(h)), "pa_alloc_create_ex")
         self._h = h
 
     def close(self):
@@ -427,6 +433,35 @@ class BlockAllocator:
         _check(lib().pa_alloc_append_slots(self._h, ids.ctypes.data, n, slots.ctypes.data, pairs.ctypes.data,
                                            ctypes.byref(npairs)), "pa_alloc_append_slots")
         return slots, pairs[: npairs.value].copy()
+
+    def add_seq_prefix(self, seq_id: int, tokens) -> int:
+        """New sequence with prompt ``tokens``; returns how many leading tokens
+        it reuses from cached blocks (their K/V need no prefill)."""
+        ids = _host_i32(list(tokens))
+        reused = ctypes.c_int(0)
+        _check(lib().pa_alloc_add_seq_prefix(self._h, seq_id, ids.ctypes.data if ids.size else None, ids.shape[0],
+                                             ctypes.byref(reused)), "pa_alloc_add_seq_prefix")
+        return reused.value
+
+    def append_tokens(self, seq_ids, token_ids):
+        """append_slots with the appended tokens' ids (for the prefix cache)."""
+        ids = _host_i32(list(seq_ids))
+        toks = _host_i32(list(token_ids))
+        n = ids.shape[0]
+        if toks.shape[0] != n:
+            raise ValueError("one token id per sequence")
+        slots = np.zeros(n, dtype=np.int64)
+        pairs = np.zeros((max(n, 1), 2), dtype=np.int32)
+        npairs = ctypes.c_int(0)
+        _check(lib().pa_alloc_append_tokens(self._h, ids.ctypes.data, toks.ctypes.data, n, slots.ctypes.data,
+                                            pairs.ctypes.data, ctypes.byref(npairs)), "pa_alloc_append_tokens")
+        return slots, pairs[: npairs.value].copy()
+
+    def prefix_stats(self):
+        """(blocks holding a cache entry, of which free)."""
+        c, f = ctypes.c_int(0), ctypes.c_int(0)
+        _check(lib().pa_alloc_prefix_stats(self._h, ctypes.byref(c), ctypes.byref(f)), "pa_alloc_prefix_stats")
+        return c.value, f.value
 
     def free_seq(self, seq_id: int):
         _check(lib().pa_alloc_free_seq(self._h, seq_id), "pa_alloc_free_seq")

@@ -169,6 +169,53 @@ def test_allocator_matches_model_on_random_operations(pa):
         alloc.close()
 
 
+def test_prefix_cache_allocator_matches_model_on_random_operations(pa):
+    """Prompts drawn from a few families over a 4-token vocabulary, so that
+    prefixes repeat, blocks are shared, freed, kept initialized, revived and
+    demoted; every step is compared with the model (slots, copy pairs, reused
+    tokens, tables, counts, cache statistics)."""
+    rng = random.Random(7)
+    for trial in range(12):
+        N = rng.randint(6, 48)
+        B = rng.choice([1, 2, 4, 16])
+        model = BlockAllocatorModel(N, B, prefix_cache=True)
+        alloc = pa.BlockAllocator(N, B, prefix_cache=True)
+        families = [[rng.randint(0, 3) for _ in range(rng.randint(1, 3 * B + 2))] for _ in range(4)]
+        nxt = 0
+        for _ in range(300):
+            live = list(model.seqs)
+            op = rng.random()
+            if op < 0.15 or not live:
+                prompt = list(rng.choice(families)) + [rng.randint(0, 3) for _ in range(rng.randint(0, B))]
+                assert alloc.add_seq_prefix(nxt, prompt) == model.add_seq_prefix(nxt, prompt)
+                nxt += 1
+            elif op < 0.22:
+                p = rng.choice(live)
+                model.fork(p, nxt)
+                alloc.fork(p, nxt)
+                nxt += 1
+            elif op < 0.30:
+                s = rng.choice(live)
+                model.free_seq(s)
+                alloc.free_seq(s)
+            else:
+                batch = rng.sample(live, rng.randint(1, len(live)))
+                ids = None if rng.random() < 0.05 else [rng.randint(0, 3) for _ in batch]
+                try:
+                    want_slots, want_pairs = model.append_slots(batch, ids)
+                except MemoryError:
+                    with pytest.raises(pa.PAError) as ei:
+                        alloc.append_slots(batch) if ids is None else alloc.append_tokens(batch, ids)
+                    assert ei.value.status == pa.PA_ERR_NO_FREE_BLOCKS
+                else:
+                    slots, pairs = alloc.append_slots(batch) if ids is None else alloc.append_tokens(batch, ids)
+                    assert slots.tolist() == want_slots
+                    assert [tuple(p) for p in pairs.tolist()] == want_pairs
+            _compare(model, alloc, range(nxt))
+            assert alloc.prefix_stats() == model.prefix_stats()
+        alloc.close()
+
+
 def test_allocator_errors(pa):
     a = pa.BlockAllocator(2, 4)
     a.add_seq(0)

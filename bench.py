@@ -197,6 +197,8 @@ WORKLOAD_TEXT = {
                  "ctx 1440, 40 heads x 128, page 256, bf16",
 }
 MIXED = ("mixed", "budget512")
+WORKLOAD_TEXT["memsim"] = ("host-only memory simulator: seeded long-tailed and short request traces, KV capacity "
+                           "32768 tokens, reservation baselines (first fit) vs paged blocks of 16")
 WORKLOAD_TEXT["swap"] = ("block swap: K/V of 8 requests x 2048 tokens, 40 heads x 128, fp16, block sizes 16..256, "
                          "GPU pool (blocks scattered) <-> pinned host pool")
 
@@ -729,6 +731,30 @@ def run_swap(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_memsim(args, rank, world):
+    """Host-only: KV memory holding tokens under Orca-Max / Orca-Pow2 /
+    Orca-Oracle reservations and under the paged allocator, on two seeded
+    synthetic traces, plus parallel-sampling and beam-search block sharing."""
+    if rank != 0:
+        return
+    from paged_kv_cache_35_gb300 import memsim
+
+    t0 = time.perf_counter()
+    n_req = max(50, min(args.steps, 600))
+    traces = {kind: memsim.synthetic_trace(kind, n_req, seed=1) for kind in ("long_tail", "short")}
+    policies = {kind: {p: memsim.simulate(p, tr, 32768).summary() for p in memsim.POLICIES}
+                for kind, tr in traces.items()}
+    sharing = memsim.sharing_over_trace(traces["long_tail"][:100])
+    value = 100.0 * policies["long_tail"]["paged"]["token_fraction"]
+    line = {"metric": "KV-cache memory holding tokens, paged blocks (time average)", "value": value, "unit": "%",
+            "n_gpus": 0, "steps": n_req, "warmup": 0, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT["memsim"], "capacity_tokens": 32768, "block_size": 16,
+                       "max_len": 2048, "requests_per_trace": n_req},
+            "policies": policies, "sharing": sharing, "wall_s": time.perf_counter() - t0}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -743,6 +769,9 @@ def main():
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    if args.workload == "memsim":
+        run_memsim(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
         return
     rank, world, local = dist_setup()
     if args.workload == "swap":

@@ -216,6 +216,42 @@ def test_prefix_cache_allocator_matches_model_on_random_operations(pa):
         alloc.close()
 
 
+def test_beam_search_fork_and_prune_match_model(pa):
+    """Beam search as the summary's section 6 describes it, on both the C++
+    allocator and the model: each step every new beam forks a surviving
+    parent, the old beams are freed (pruned branches return their blocks at
+    reference count 0) and every beam appends a token (copy-on-write of a
+    shared partial block).  Compared after every step."""
+    rng = random.Random(11)
+    for width, B in ((2, 4), (4, 16), (6, 1)):
+        model = BlockAllocatorModel(400, B)
+        alloc = pa.BlockAllocator(400, B)
+        for m in (model, alloc):
+            m.add_seq(0)
+        for _ in range(37):
+            assert alloc.append_slots([0])[0].tolist() == model.append_slots([0])[0]
+        beams, nxt = [0], 1
+        for _ in range(60):
+            parents = [rng.choice(beams) for _ in range(width)]
+            new = list(range(nxt, nxt + width))
+            nxt += width
+            for p_, c in zip(parents, new):
+                model.fork(p_, c)
+                alloc.fork(p_, c)
+            for b in beams:
+                model.free_seq(b)
+                alloc.free_seq(b)
+            want_slots, want_pairs = model.append_slots(new)
+            slots, pairs = alloc.append_slots(new)
+            assert slots.tolist() == want_slots and [tuple(x) for x in pairs.tolist()] == want_pairs
+            beams = new
+            _compare(model, alloc, beams)
+        # only the surviving beams' blocks are held
+        held = {b for s in beams for b in model.table(s)}
+        assert alloc.num_free() == 400 - len(held)
+        alloc.close()
+
+
 def test_allocator_errors(pa):
     a = pa.BlockAllocator(2, 4)
     a.add_seq(0)

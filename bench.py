@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per pa_decode call on this workload, from the ncu
 # capture summarised in profiles/; valid only for the decode kernel source
 # whose sha256 prefix is given (otherwise reported as null).
-TRAFFIC = {"bytes_per_launch": 1488348520, "kernel_sha256_prefix": "2a405fce46e2aecc",
+TRAFFIC = {"bytes_per_launch": 1488220640, "kernel_sha256_prefix": "40eb1ddd4985d1ca",
            "source": "profiles/decode_kernel_llama13b_b64.md"}
 
 

@@ -226,12 +226,15 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q, const void
  * cu_q_lens: device int32 [num_chunks + 1], cu_q_lens[0] == 0, non-decreasing.
  * ctx_before: device int32 [num_chunks].
  * total_q: number of rows of q and out (== cu_q_lens[num_chunks]).
- * max_q_len: host upper bound of any chunk's length (sizes the grid).
+ * max_q_len: host upper bound of any chunk's length (sizes the work list).
  * Requires head_dim 128, and block_size a multiple of 16 that divides 128 or
  * is a multiple of 128.  Runs on the tensor cores (tcgen05.mma, accumulators
  * in tensor memory, tiles moved by TMA).  A chunk whose context runs past
  * its table sets PA_FLAG_BAD_LENGTH and is skipped; a table entry outside the
  * pool sets PA_FLAG_BAD_BLOCK and its tokens are left out.
+ * Persistent grid (one CTA per SM).  A kernel launched behind it with
+ * programmatic stream serialization may start while it runs and must wait
+ * (griddepcontrol.wait) before reading its output.
  */
 int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens,
                      const int32_t* ctx_before, const void* k_pool, const void* v_pool,
@@ -249,22 +252,14 @@ int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_
  *    chosen automatically); pf_* and the chunk arguments those of
  *    pa_prefill_chunk; pools, num_heads, head_dim, block_size, num_blocks,
  *    scale, dtype and err_flag are shared.  head_dim must be 128 (prefill).
- *  - The prefill runs on `aux_stream` on at most `prefill_sms` SMs
- *    (<= 0: PA_MIXED_PREFILL_SHARE percent of them), launched first; the
- *    decode runs on `stream` on the rest of the GPU.  aux_stream first waits
- *    for the work queued on `stream` before the call; `stream` then waits for
- *    the prefill, so work queued on `stream` after the call sees both outputs.
- *    aux_stream must be a stream other than `stream` (NULL is rejected).
- *    Give aux_stream a higher priority than `stream`
- *    (cudaStreamCreateWithPriority): when steps are queued back to back both
- *    parts become ready at the same moment, and the priority makes the block
- *    scheduler place the prefill's CTAs first; otherwise the decode's grid
- *    may fill every SM and the two parts run one after the other (correct,
- *    but without the overlap).
+ *  - On `stream`: the decode's planning kernel, then the prefill's persistent
+ *    grid on at most `prefill_sms` SMs (<= 0: PA_MIXED_PREFILL_SHARE percent
+ *    of them), then the decode kernel as a programmatic dependent of the
+ *    prefill: it starts as soon as the prefill's CTAs are resident and fills
+ *    the remaining SMs.  Work queued on `stream` afterwards sees both outputs.
  *  - Outputs: the same values as pa_decode and pa_prefill_chunk give.
  *  - All arguments of both parts are checked before anything is launched.
- *    Events are created and destroyed per call; nothing is allocated on the
- *    device.
+ *    With no chunks it is pa_decode; with no sequences, pa_prefill_chunk.
  */
 #define PA_MIXED_PREFILL_SHARE 45
 int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int32_t* dec_block_tables,
@@ -273,7 +268,7 @@ int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int
                   const int32_t* cu_q_lens, const int32_t* ctx_before, const int32_t* pf_block_tables,
                   int pf_max_blocks_per_seq, int num_chunks, int total_q, int max_q_len, const void* k_pool,
                   const void* v_pool, int num_heads, int head_dim, int block_size, int num_blocks, float scale,
-                  int dtype, int prefill_sms, int32_t* err_flag, void* stream, void* aux_stream);
+                  int dtype, int prefill_sms, int32_t* err_flag, void* stream);
 
 /*
  * Decode graphs -- pa_decode recorded once per padded batch shape and

@@ -55,7 +55,7 @@ SIGNATURES = {
     "pa_decode_static_scratch": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P], _I),
     "pa_prefill_chunk": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P], _I),
     "pa_mixed_step": ([_P, _I, _P, _P, _I, _P, _I, _I, _P, _Z, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I,
-                       _I, _I, _F, _I, _I, _P, _P, _P], _I),
+                       _I, _I, _F, _I, _I, _P, _P], _I),
     "pa_swap_blocks": ([_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pa_decode_graphs_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _Z),
     "pa_decode_graphs_create": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _I, _I, _P,
@@ -285,12 +285,11 @@ def pa_prefill_chunk(out, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables
 
 
 def pa_mixed_step(dec_out, dec_q, dec_block_tables, context_lens, max_context_len, workspace, pf_out, pf_q,
-                  cu_q_lens, ctx_before, pf_block_tables, max_q_len, k_pool, v_pool, scale, err_flag, aux_stream,
+                  cu_q_lens, ctx_before, pf_block_tables, max_q_len, k_pool, v_pool, scale, err_flag,
                   prefill_sms=0, stream=None):
     """Decode of dec_q [S][H][D] and prefill of the chunks in pf_q [total][H][D]
-    over the same pools, concurrently: the prefill on aux_stream (a
-    torch.cuda.Stream other than `stream`, created with a higher priority,
-    e.g. torch.cuda.Stream(priority=-1)), the decode on `stream`."""
+    over the same pools, running concurrently on `stream` (the prefill on at
+    most prefill_sms SMs, 0 = the default share)."""
     NB, H, B, D = k_pool.shape
     S = dec_q.shape[0]
     T = pf_q.shape[0]
@@ -313,7 +312,7 @@ def pa_mixed_step(dec_out, dec_q, dec_block_tables, context_lens, max_context_le
         _dev(ctx_before, "ctx_before", torch.int32), _dev(pf_block_tables, "pf_block_tables", torch.int32),
         pf_block_tables.shape[1], C, T, int(max_q_len), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
         H, D, B, NB, float(scale), _kv_code(k_pool), int(prefill_sms), _dev(err_flag, "err_flag", torch.int32),
-        _stream(stream), _stream(aux_stream))
+        _stream(stream))
     _check(st, "pa_mixed_step")
 
 

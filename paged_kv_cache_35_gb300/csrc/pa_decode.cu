@@ -99,6 +99,8 @@ struct DecodeArgs {
   float2* part_ml; // [S][H][max_parts] (max, sum) in log2 units
   float* part_o;   // [S][H][max_parts][D] normalised partial outputs
   int32_t* err_flag;
+  int dep_wait;    // 1: wait for the planning kernel (launched right before); 0: it completed before the
+                   // kernel this one was launched behind
 };
 
 template <int D, typename T>
@@ -539,7 +541,7 @@ __global__ void __launch_bounds__(kDecodeThreads, PA_DECODE_MIN_CTAS) decode_ker
     fence_barrier_init();
   }
   __syncthreads();
-  griddep_wait();  // the planning kernel's list and counters are visible from here
+  if (a.dep_wait) griddep_wait();  // the planning kernel's list and counters are visible from here
   if (warp == kSchedulerWarp) {
     run_scheduler<D, T>(a, sm, lane);
   } else if (warp == kProducerWarp) {
@@ -585,7 +587,7 @@ int resolve_partition(int S, int H, int max_ctx, int partition_size) {
 }
 
 template <int D, typename T>
-int launch_decode(const pa::DecodeArgs& a, cudaStream_t stream) {
+int configure_decode(int* occ_out) {
   using Smem = pa::DecodeSmem<D, T>;
   const int smem = (int)sizeof(Smem);
   int dev = 0;
@@ -604,22 +606,35 @@ int launch_decode(const pa::DecodeArgs& a, cudaStream_t stream) {
     occupancy[dev] = occ > 0 ? occ : 1;
     configured[dev] = 1;
   }
-  const int sms = pa_host::device_sm_count();
-  if (sms <= 0) return PA_ERR_CUDA;
+  *occ_out = occupancy[dev];
+  return PA_OK;
+}
 
+template <int D>
+int launch_plan(const pa::DecodeArgs& a, cudaStream_t stream) {
   const int nb = a.partition_size / pa::kChunk;
   pa::plan_kernel<D><<<1, pa::kPlanThreads, 3 * nb * sizeof(int), stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 
+// The persistent decode kernel, launched as a programmatic dependent of the
+// kernel before it on the stream.
+template <int D, typename T>
+int launch_main(const pa::DecodeArgs& a, cudaStream_t stream) {
+  int occ = 0;
+  const int st = configure_decode<D, T>(&occ);
+  if (st != PA_OK) return st;
+  const int sms = pa_host::device_sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
   const long long max_units = (long long)a.num_seqs * a.num_heads * a.max_parts;
-  long long grid = (long long)sms * occupancy[dev];
+  long long grid = (long long)sms * occ;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(pa::kDecodeThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = sizeof(pa::DecodeSmem<D, T>);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -628,6 +643,30 @@ int launch_decode(const pa::DecodeArgs& a, cudaStream_t stream) {
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, pa::decode_kernel<D, T>, a) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
+}
+
+// Planning kernel, then the decode kernel behind it.
+template <int D, typename T>
+int launch_decode(const pa::DecodeArgs& a, cudaStream_t stream) {
+  int occ = 0;
+  int st = configure_decode<D, T>(&occ);  // attribute calls before the first launch of the pair
+  if (st != PA_OK) return st;
+  st = launch_plan<D>(a, stream);
+  if (st != PA_OK) return st;
+  return launch_main<D, T>(a, stream);
+}
+
+int configure_any(int head_dim, int dtype) {
+  int occ = 0;
+  if (head_dim == 128)
+    return dtype == PA_F16 ? configure_decode<128, __half>(&occ) : configure_decode<128, __nv_bfloat16>(&occ);
+  return dtype == PA_F16 ? configure_decode<64, __half>(&occ) : configure_decode<64, __nv_bfloat16>(&occ);
+}
+
+int launch_main_any(const pa::DecodeArgs& a, int head_dim, int dtype, cudaStream_t s) {
+  if (head_dim == 128)
+    return dtype == PA_F16 ? launch_main<128, __half>(a, s) : launch_main<128, __nv_bfloat16>(a, s);
+  return dtype == PA_F16 ? launch_main<64, __half>(a, s) : launch_main<64, __nv_bfloat16>(a, s);
 }
 
 // Checks pa_decode's arguments and fills the kernel arguments; launches
@@ -682,6 +721,7 @@ int decode_setup(void* out, int out_dtype, const void* q, const void* k_pool, co
   a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
   a.part_o = reinterpret_cast<float*>(ws + w.o);
   a.err_flag = err_flag;
+  a.dep_wait = 1;
   return PA_OK;
 }
 
@@ -736,6 +776,61 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
     return dtype == PA_F16 ? launch_decode<128, __half>(a, s) : launch_decode<128, __nv_bfloat16>(a, s);
   }
   return dtype == PA_F16 ? launch_decode<64, __half>(a, s) : launch_decode<64, __nv_bfloat16>(a, s);
+}
+
+// pa_mixed_step: one step of a batch that mixes decode sequences and prefill
+// chunks, the two parts running at the same time.  The continuous-batching
+// page ("연속 배치 처리 아키텍처", "Chunked prefill" and the scheduler) fills a
+// step's token budget with decode tokens and prefill chunks and runs them as
+// one forward pass.  The decode streams K/V from HBM with CUDA-core
+// arithmetic; the prefill is bound by the tensor cores; so they overlap:
+// the planning kernel runs first, then the prefill's persistent grid, capped
+// to a share of the SMs, then the decode kernel as a programmatic dependent
+// of the prefill.  Every prefill CTA releases its dependents as it starts,
+// so the decode grid fills the SMs the prefill left free; the decode skips
+// its wait on the planning kernel, which completed before the prefill began.
+int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int32_t* dec_block_tables,
+                  int dec_max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+                  void* workspace, size_t workspace_bytes, void* pf_out, int pf_out_dtype, const void* pf_q,
+                  const int32_t* cu_q_lens, const int32_t* ctx_before, const int32_t* pf_block_tables,
+                  int pf_max_blocks_per_seq, int num_chunks, int total_q, int max_q_len, const void* k_pool,
+                  const void* v_pool, int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                  int dtype, int prefill_sms, int32_t* err_flag, void* stream) {
+  pa::DecodeArgs a;
+  bool dec_empty = false;
+  int st = decode_setup(dec_out, dec_out_dtype, dec_q, k_pool, v_pool, dec_block_tables, dec_max_blocks_per_seq,
+                        context_lens, max_context_len, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
+                        dtype, workspace, workspace_bytes, 0, err_flag, a, dec_empty);
+  if (st != PA_OK) return st;
+  st = pa_host::prefill_check(pf_out, pf_out_dtype, pf_q, cu_q_lens, ctx_before, k_pool, v_pool, pf_block_tables,
+                              pf_max_blocks_per_seq, num_chunks, total_q, max_q_len, num_heads, head_dim, block_size,
+                              num_blocks, scale, dtype, err_flag);
+  if (st != PA_OK) return st;
+  const bool pf_empty = num_chunks == 0 || total_q == 0 || max_q_len == 0;
+  const int sms = pa_host::device_sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+  int cap = prefill_sms > 0 ? (prefill_sms < sms ? prefill_sms : sms) : (sms * PA_MIXED_PREFILL_SHARE + 50) / 100;
+  if (cap < 1) cap = 1;
+  auto prefill = [&](int ctas) {
+    return pa_host::prefill_launch(pf_out, pf_out_dtype, pf_q, cu_q_lens, ctx_before, k_pool, v_pool,
+                                   pf_block_tables, pf_max_blocks_per_seq, num_chunks, total_q, max_q_len,
+                                   num_heads, head_dim, block_size, num_blocks, scale, dtype, err_flag, ctas, stream);
+  };
+  if (dec_empty) return pf_empty ? PA_OK : prefill(0);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (pf_empty) {
+    return head_dim == 128
+               ? (dtype == PA_F16 ? launch_decode<128, __half>(a, s) : launch_decode<128, __nv_bfloat16>(a, s))
+               : (dtype == PA_F16 ? launch_decode<64, __half>(a, s) : launch_decode<64, __nv_bfloat16>(a, s));
+  }
+  st = configure_any(head_dim, dtype);
+  if (st != PA_OK) return st;
+  st = head_dim == 128 ? launch_plan<128>(a, s) : launch_plan<64>(a, s);
+  if (st != PA_OK) return st;
+  st = prefill(cap);
+  if (st != PA_OK) return st;
+  a.dep_wait = 0;
+  return launch_main_any(a, head_dim, dtype, s);
 }
 
 }  // extern "C"

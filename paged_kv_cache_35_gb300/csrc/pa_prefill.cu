@@ -367,6 +367,10 @@ template <typename T>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+  // a kernel launched behind this one as a programmatic dependent may start
+  // as soon as every CTA is resident (pa_mixed_step's decode); it must not
+  // read this kernel's output without waiting for it
+  griddep_launch_dependents();
   extern __shared__ uint8_t pf_smem_raw[];
   const uint32_t raw = smem_u32(pf_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;

@@ -1,9 +1,10 @@
 """pa_mixed_step: decode and chunked prefill of one mixed batch run
-concurrently (prefill on a second stream with a capped grid, decode on the
-caller's stream).  Its outputs must be bit-identical to pa_decode and
-pa_prefill_chunk called one after the other, for any prefill SM share, and
+concurrently on one stream (the prefill's grid capped to a share of the
+SMs, the decode launched behind it as a programmatic dependent).  Its
+outputs must be bit-identical to pa_decode and pa_prefill_chunk called one
+after the other, for any prefill SM share and with either part empty, and
 match the oracle; the stream ordering it promises is exercised by queueing
-the inputs' scatter and the outputs' readers on the caller's stream without
+the inputs' scatter and the outputs' readers on a non-default stream without
 any host synchronisation in between."""
 from __future__ import annotations
 
@@ -68,11 +69,11 @@ class Step:
         pa.pa_prefill_chunk(pout, m.chunk_q, self.cu, self.cb, w.k_pool, w.v_pool, self.ctab, self.mq, w.scale, err)
         return dout, pout
 
-    def mixed(self, pa, err, aux, prefill_sms=0, stream=None):
+    def mixed(self, pa, err, prefill_sms=0, stream=None):
         w, m = self.w, self.m
         dout, pout = self.outputs()
         pa.pa_mixed_step(dout, w.q, self.tables, self.ctx, self.mx, self.ws, pout, m.chunk_q, self.cu, self.cb,
-                         self.ctab, self.mq, w.k_pool, w.v_pool, w.scale, err, aux, prefill_sms=prefill_sms,
+                         self.ctab, self.mq, w.k_pool, w.v_pool, w.scale, err, prefill_sms=prefill_sms,
                          stream=stream)
         return dout, pout
 
@@ -85,9 +86,8 @@ def test_mixed_step_is_bit_identical_to_separate_calls(pa):
     pa.pa_reshape_and_cache(st.k_new, st.v_new, w.k_pool, w.v_pool, st.slots, err)
     ref_d, ref_p = st.separate(pa, err)
     assert pa.pa_get_error(err) == 0
-    aux = torch.cuda.Stream(priority=-1)
     for sms in (0, 1, 24, 76, 10000):  # auto share, one SM, a few, half, more than the GPU has
-        d, p = st.mixed(pa, err, aux, prefill_sms=sms)
+        d, p = st.mixed(pa, err, prefill_sms=sms)
         assert pa.pa_get_error(err) == 0
         assert torch.equal(d.view(torch.int16), ref_d.view(torch.int16)), sms
         assert torch.equal(p.view(torch.int16), ref_p.view(torch.int16)), sms
@@ -103,11 +103,11 @@ def test_mixed_step_budget512_matches_oracle(pa):
     chunk_k, chunk_v, chunk_q = m.chunk_k.cpu(), m.chunk_v.cpu(), m.chunk_q.cpu()
     st = Step(pa, m)
     err = pa.new_error_flag()
-    main, aux = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    main = torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(main):
         pa.pa_reshape_and_cache(st.k_new, st.v_new, w.k_pool, w.v_pool, st.slots, err, stream=main)
-        d, p = st.mixed(pa, err, aux, stream=main)
+        d, p = st.mixed(pa, err, stream=main)
         d_host = d.to("cpu", non_blocking=False)
         p_host = p.to("cpu", non_blocking=False)
     assert pa.pa_get_error(err, main) == 0
@@ -130,21 +130,48 @@ def test_mixed_step_budget512_matches_oracle(pa):
 
 
 def test_mixed_step_refuses_bad_arguments_before_launching(pa):
+    """A bad argument of either part: nothing may run, not even the other part."""
     m = W.mixed_prefill(device="cuda", num_decode=4, chunk_len=64, ctx_before=(100,))
     st = Step(pa, m)
     err = pa.new_error_flag()
-    s = torch.cuda.current_stream()
-    with pytest.raises(pa.PAError) as e:  # aux stream == caller stream
-        st.mixed(pa, err, s, stream=s)
-    assert e.value.status == pa.PA_ERR_INVALID_ARG
-    # a decode workspace that is too small: nothing may run, not even the prefill
     w = m.decode
     d, p = st.outputs()
-    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")  # decode workspace too small
     with pytest.raises(pa.PAError) as e:
         pa.pa_mixed_step(d, w.q, st.tables, st.ctx, st.mx, small, p, m.chunk_q, st.cu, st.cb, st.ctab, st.mq,
-                         w.k_pool, w.v_pool, w.scale, err, torch.cuda.Stream())
+                         w.k_pool, w.v_pool, w.scale, err)
     assert e.value.status == pa.PA_ERR_WORKSPACE
+    with pytest.raises(pa.PAError) as e:  # a negative chunk-length bound
+        pa.pa_mixed_step(d, w.q, st.tables, st.ctx, st.mx, st.ws, p, m.chunk_q, st.cu, st.cb, st.ctab, -1,
+                         w.k_pool, w.v_pool, w.scale, err)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.isnan(p.float()).all() and torch.isnan(d.float()).all()
     assert pa.pa_get_error(err) == 0
+
+
+def test_mixed_step_with_one_part_empty(pa):
+    """No chunks: it is pa_decode; no sequences: it is pa_prefill_chunk."""
+    m = W.mixed_prefill(device="cuda", num_decode=6, chunk_len=200, ctx_before=(300,))
+    st = Step(pa, m)
+    w = m.decode
+    dev = torch.device("cuda")
+    err = pa.new_error_flag()
+    pa.pa_reshape_and_cache(st.k_new, st.v_new, w.k_pool, w.v_pool, st.slots, err)
+    ref_d, ref_p = st.separate(pa, err)
+    H, D = w.num_heads, w.head_dim
+    d, _ = st.outputs()
+    no_q = torch.empty(0, H, D, dtype=w.q.dtype, device=dev)
+    no_out = torch.empty(0, H, D, dtype=torch.bfloat16, device=dev)
+    zero_cu = torch.zeros(1, dtype=torch.int32, device=dev)
+    no_cb = torch.empty(0, dtype=torch.int32, device=dev)
+    pa.pa_mixed_step(d, w.q, st.tables, st.ctx, st.mx, st.ws, no_out, no_q, zero_cu, no_cb, st.ctab, 0,
+                     w.k_pool, w.v_pool, w.scale, err)
+    _, p = st.outputs()
+    no_tables = torch.empty(0, w.max_blocks_per_seq, dtype=torch.int32, device=dev)
+    no_ctx = torch.empty(0, dtype=torch.int32, device=dev)
+    pa.pa_mixed_step(no_out, no_q, no_tables, no_ctx, 0, st.ws, p, m.chunk_q, st.cu, st.cb, st.ctab, st.mq,
+                     w.k_pool, w.v_pool, w.scale, err)
+    assert pa.pa_get_error(err) == 0
+    assert torch.equal(d.view(torch.int16), ref_d.view(torch.int16))
+    assert torch.equal(p.view(torch.int16), ref_p.view(torch.int16))

@@ -227,8 +227,7 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q, const void
  * ctx_before: device int32 [num_chunks].
  * total_q: number of rows of q and out (== cu_q_lens[num_chunks]).
  * max_q_len: host upper bound of any chunk's length (sizes the work list).
- * Requires head_dim 128, and block_size a multiple of 16 that divides 128 or
- * is a multiple of 128.  Runs on the tensor cores (tcgen05.mma, accumulators
+ * Requires head_dim 128 and block_size a multiple of 16 (up to 65536).  Runs on the tensor cores (tcgen05.mma, accumulators
  * in tensor memory, tiles moved by TMA).  A chunk whose context runs past
  * its table sets PA_FLAG_BAD_LENGTH and is skipped; a table entry outside the
  * pool sets PA_FLAG_BAD_BLOCK and its tokens are left out.

@@ -115,7 +115,7 @@ struct PrefillArgs {
   int num_heads;
   int block_size;
   int num_blocks;
-  int rows_per_load;  // min(block_size, 128)
+  int rows_per_load;  // gcd(block_size, 128): a piece of that many keys never straddles a page
   int rpl_shift;      // log2(rows_per_load)
   int pool_rows;      // num_blocks * H * B: any row at or past it reads zeros
   int num_chunks;
@@ -857,8 +857,7 @@ int prefill_setup(void* out, int out_dtype, const void* q, const int32_t* cu_q_l
   empty = false;
   if (!pa_host::is_kv_dtype(dtype) || !pa_host::is_out_dtype(out_dtype)) return PA_ERR_UNSUPPORTED;
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size <= 0 || block_size % 16 != 0 || !(128 % block_size == 0 || block_size % 128 == 0))
-    return PA_ERR_UNSUPPORTED;
+  if (block_size <= 0 || block_size % 16 != 0 || block_size > 65536) return PA_ERR_UNSUPPORTED;
   if (num_chunks < 0 || total_q < 0 || max_q_len < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
     return PA_ERR_INVALID_ARG;
   if (num_chunks == 0 || total_q == 0 || max_q_len == 0) {
@@ -890,7 +889,8 @@ int prefill_setup(void* out, int out_dtype, const void* q, const int32_t* cu_q_l
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PA_ERR_CUDA;
   }
-  const int rows_per_load = block_size < 128 ? block_size : 128;
+  int rows_per_load = 128;  // gcd(block_size, 128), a power of two from 16 to 128
+  while (block_size % rows_per_load != 0) rows_per_load /= 2;
   for (int which = 0; which < 2; ++which) {
     cuuint64_t dims[2] = {128, (cuuint64_t)pool_rows};
     cuuint64_t strides[1] = {128 * 2};

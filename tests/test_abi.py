@@ -76,13 +76,15 @@ def test_bad_arguments_are_rejected_before_launch(pa):
     assert L.pa_decode(*args) == pa.PA_ERR_INVALID_ARG
     args[9] = 0  # no sequences: nothing to do
     assert L.pa_decode(*args) == pa.PA_OK
-    # prefill: head_dim 64 unsupported, block size 48 unsupported
-    pargs = [fake, pa.PA_BF16, fake, fake, fake, fake, fake, fake, 8, 2, 100, 64, 4, 64, 16, 8, 0.1, pa.PA_BF16, fake,
+    # prefill (every case must be refused before a launch: the pointers are fake):
+    # head_dim 96, block size 40 (not a multiple of 16), block size past 65536
+    pargs = [fake, pa.PA_BF16, fake, fake, fake, fake, fake, fake, 8, 2, 100, 64, 4, 96, 16, 8, 0.1, pa.PA_BF16, fake,
              None]
     assert L.pa_prefill_chunk(*pargs) == pa.PA_ERR_UNSUPPORTED
     pargs[13] = 128
-    pargs[14] = 48
-    assert L.pa_prefill_chunk(*pargs) == pa.PA_ERR_UNSUPPORTED
+    for bad_block in (40, 65552):
+        pargs[14] = bad_block
+        assert L.pa_prefill_chunk(*pargs) == pa.PA_ERR_UNSUPPORTED
     # scatter / copy with nothing to do
     assert L.pa_reshape_and_cache(fake, fake, fake, fake, fake, 0, 4, 64, 16, 8, pa.PA_F16, fake, None) == pa.PA_OK
     assert L.pa_copy_blocks(fake, fake, fake, 0, 4, 64, 16, 8, pa.PA_F16, fake, None) == pa.PA_OK

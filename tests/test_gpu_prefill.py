@@ -71,7 +71,7 @@ def test_prefill_small_ragged_bf16(pa, out_dtype):
     assert_attn_close(out, ref, out_dtype, "prefill bf16")
 
 
-@pytest.mark.parametrize("B", [16, 32, 128, 256])
+@pytest.mark.parametrize("B", [16, 32, 48, 80, 128, 144, 256, 384])
 def test_prefill_block_sizes(pa, B):
     m = W.small_prefill(chunk_lens=(200, 64), ctx_before=(300, 0), H=2, B=B)
     out, flags, _, _ = run_prefill(pa, m, "f32")

@@ -227,7 +227,7 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q, const void
  * ctx_before: device int32 [num_chunks].
  * total_q: number of rows of q and out (== cu_q_lens[num_chunks]).
  * max_q_len: host upper bound of any chunk's length (sizes the work list).
- * Requires head_dim 128 and block_size a multiple of 16 (up to 65536).  Runs on the tensor cores (tcgen05.mma, accumulators
+ * Requires head_dim 64 or 128 and block_size a multiple of 16 (up to 65536).  Runs on the tensor cores (tcgen05.mma, accumulators
  * in tensor memory, tiles moved by TMA).  A chunk whose context runs past
  * its table sets PA_FLAG_BAD_LENGTH and is skipped; a table entry outside the
  * pool sets PA_FLAG_BAD_BLOCK and its tokens are left out.
@@ -250,7 +250,7 @@ int pa_prefill_chunk(void* out, int out_dtype, const void* q, const int32_t* cu_
  *  - dec_* and the decode arguments are those of pa_decode (partition size
  *    chosen automatically); pf_* and the chunk arguments those of
  *    pa_prefill_chunk; pools, num_heads, head_dim, block_size, num_blocks,
- *    scale, dtype and err_flag are shared.  head_dim must be 128 (prefill).
+ *    scale, dtype and err_flag are shared.
  *  - On `stream`: the decode's planning kernel, then the prefill's persistent
  *    grid on at most `prefill_sms` SMs (<= 0: PA_MIXED_PREFILL_SHARE percent
  *    of them), then the decode kernel as a programmatic dependent of the

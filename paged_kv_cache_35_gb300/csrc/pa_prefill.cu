@@ -64,7 +64,6 @@ namespace pa {
 
 constexpr int kPfRows = 128;   // query rows per tile (MMA M)
 constexpr int kPfKeys = 128;   // keys per tile (N of S = Q K^T, K of O += P V)
-constexpr int kPfD = 128;      // head_dim
 constexpr int kPfThreads = 320;
 constexpr int kPfMmaWarp = 8;
 constexpr int kPfLoadWarp = 9;
@@ -363,10 +362,14 @@ __device__ __forceinline__ long long pf_round_pos(int r) {
   return (long long)r * G + ((r & 1) ? (G - 1 - b) : b);
 }
 
-template <typename T>
+// D = head_dim, 64 or 128: tiles are D / 64 swizzled 64-column halves.
+template <typename T, int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  constexpr int kHalves = D / 64;
+  constexpr uint32_t kLoadBytes = kHalves * kHalfBytes;  // bytes of one loaded Q, K or V tile
   // a kernel launched behind this one as a programmatic dependent may start
   // as soon as every CTA is resident (pa_mixed_step's decode); it must not
   // read this kernel's output without waiting for it
@@ -462,8 +465,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (lane == 0) {  // the query tile, once the previous item's last S = Q K^T is done with the buffer
         wok = mbar_wait(&bars.q_empty, (k & 1) ^ 1, abort_flag, a.err_flag);
         if (wok) {
-          mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
-          for (int hf = 0; hf < 2; ++hf)
+          mbar_arrive_expect_tx(&bars.q_full, kLoadBytes);
+          for (int hf = 0; hf < kHalves; ++hf)
             tma_load_3d(base + kOffQ + hf * kHalfBytes, &tm_q, hf * 64, it.h, it.q0 + it.row0, &bars.q_full);
         }
       }
@@ -491,13 +494,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ok = false;
             break;
           }
-          if (lane == 0) mbar_arrive_expect_tx(&bars.k_full[stg], kTileBytes);
+          if (lane == 0) mbar_arrive_expect_tx(&bars.k_full[stg], kLoadBytes);
           for (int pc = 0; pc < loads; ++pc) {
             const int rr = __shfl_sync(0xffffffffu, row, pc);
             if (lane == 0) {
               const uint32_t dst = base + kOffK + stg * kTileBytes + (uint32_t)pc * rpl * 128u;
               tma_load_2d(dst, &tm_k, 0, rr, &bars.k_full[stg]);
-              tma_load_2d(dst + kHalfBytes, &tm_k, 64, rr, &bars.k_full[stg]);
+              if (kHalves == 2) tma_load_2d(dst + kHalfBytes, &tm_k, 64, rr, &bars.k_full[stg]);
             }
           }
           ++k_issued;
@@ -510,13 +513,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ok = false;
             break;
           }
-          if (lane == 0) mbar_arrive_expect_tx(&bars.v_full[stg], kTileBytes);
+          if (lane == 0) mbar_arrive_expect_tx(&bars.v_full[stg], kLoadBytes);
           for (int pc = 0; pc < loads; ++pc) {
             const int rr = __shfl_sync(0xffffffffu, prev_row, pc);
             if (lane == 0) {
               const uint32_t dst = base + kOffV + stg * kTileBytes + (uint32_t)pc * rpl * 128u;
               tma_load_2d(dst, &tm_v, 0, rr, &bars.v_full[stg]);
-              tma_load_2d(dst + kHalfBytes, &tm_v, 64, rr, &bars.v_full[stg]);
+              if (kHalves == 2) tma_load_2d(dst + kHalfBytes, &tm_v, 64, rr, &bars.v_full[stg]);
             }
           }
           ++v_issued;
@@ -556,7 +559,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const uint64_t kdesc = smem_desc_sw128(base + kOffK + (x % kKStages) * kTileBytes, 16, 1024);
           const uint32_t d = tmem + tmem_s(x & 1);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < 4 * kHalves; ++kk) {  // K = head_dim in steps of 16
             const uint32_t koff = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
             umma_f16(d, qdesc + koff, kdesc + koff, a.idesc_s, kk > 0);
           }
@@ -703,7 +706,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_st16(pw + 48, lw + 16);
         if (any_resc) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < D / 32; ++cc) {
             float o[32];
             tmem_ld32(o_mine + cc * 32, o);
 #pragma unroll
@@ -725,7 +728,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
               *reinterpret_cast<uint4*>(vbuf + r * 128 + ch * 16) = z;
-              *reinterpret_cast<uint4*>(vbuf + kHalfBytes + r * 128 + ch * 16) = z;
+              if (kHalves == 2) *reinterpret_cast<uint4*>(vbuf + kHalfBytes + r * 128 + ch * 16) = z;
             }
           }
           fence_proxy_async_smem();
@@ -763,12 +766,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float c0w = w0 * inv, c1w = w1 * inv;
       const bool store = qrow < it.n_c;
-      const size_t obase = ((size_t)(it.q0 + qrow) * H + it.h) * kPfD + col0;
+      const int ocol0 = half * (D / 2);  // this thread writes output columns ocol0 .. ocol0 + D/2 - 1
+      const size_t obase = ((size_t)(it.q0 + qrow) * H + it.h) * D + ocol0;
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
         float oa[32], ob[32];
-        tmem_ld32(lane_addr + tmem_o(0) + col0 + cc * 32, oa);
-        tmem_ld32(lane_addr + tmem_o(1) + col0 + cc * 32, ob);
+        tmem_ld32(lane_addr + tmem_o(0) + ocol0 + cc * 32, oa);
+        tmem_ld32(lane_addr + tmem_o(1) + ocol0 + cc * 32, ob);
         float o[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = c0w * oa[i] + c1w * ob[i];
@@ -835,14 +839,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A/B in
-// `ab_format` (0 = fp16, 1 = bf16), M = 128, N = 128, B K-major or MN-major.
-uint32_t make_idesc(uint32_t ab_format, bool b_mn_major) {
+// `ab_format` (0 = fp16, 1 = bf16), M = 128, N = n, B K-major or MN-major.
+uint32_t make_idesc(uint32_t ab_format, bool b_mn_major, int n) {
   uint32_t d = 0;
   d |= 1u << 4;                 // D format: f32
   d |= ab_format << 7;          // A format
   d |= ab_format << 10;         // B format
   d |= (b_mn_major ? 1u : 0u) << 16;
-  d |= (uint32_t)(128 >> 3) << 17;  // N
+  d |= (uint32_t)(n >> 3) << 17;  // N
   d |= (uint32_t)(128 >> 4) << 24;  // M
   return d;
 }
@@ -856,7 +860,7 @@ int prefill_setup(void* out, int out_dtype, const void* q, const int32_t* cu_q_l
                   CUtensorMap& tm_k, CUtensorMap& tm_v, bool& empty) {
   empty = false;
   if (!pa_host::is_kv_dtype(dtype) || !pa_host::is_out_dtype(out_dtype)) return PA_ERR_UNSUPPORTED;
-  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (block_size <= 0 || block_size % 16 != 0 || block_size > 65536) return PA_ERR_UNSUPPORTED;
   if (num_chunks < 0 || total_q < 0 || max_q_len < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
     return PA_ERR_INVALID_ARG;
@@ -880,8 +884,8 @@ int prefill_setup(void* out, int out_dtype, const void* q, const int32_t* cu_q_l
   if (encode == nullptr) return PA_ERR_CUDA;
   const CUtensorMapDataType tdt = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   {
-    cuuint64_t dims[3] = {128, (cuuint64_t)num_heads, (cuuint64_t)total_q};
-    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)num_heads * 128 * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
     cuuint32_t box[3] = {64, 1, 128};
     cuuint32_t es[3] = {1, 1, 1};
     if (encode(&tm_q, tdt, 3, const_cast<void*>(q), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -892,8 +896,8 @@ int prefill_setup(void* out, int out_dtype, const void* q, const int32_t* cu_q_l
   int rows_per_load = 128;  // gcd(block_size, 128), a power of two from 16 to 128
   while (block_size % rows_per_load != 0) rows_per_load /= 2;
   for (int which = 0; which < 2; ++which) {
-    cuuint64_t dims[2] = {128, (cuuint64_t)pool_rows};
-    cuuint64_t strides[1] = {128 * 2};
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)pool_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)rows_per_load};
     cuuint32_t es[2] = {1, 1};
     if (encode(which ? &tm_v : &tm_k, tdt, 2, const_cast<void*>(which ? v_pool : k_pool), dims, strides, box, es,
@@ -916,8 +920,8 @@ int prefill_setup(void* out, int out_dtype, const void* q, const int32_t* cu_q_l
   a.pool_rows = (int)pool_rows;
   a.qscale = scale * 1.4426950408889634f;
   const uint32_t fmt = dtype == PA_BF16 ? 1u : 0u;
-  a.idesc_s = make_idesc(fmt, false);
-  a.idesc_pv = make_idesc(fmt, true);
+  a.idesc_s = make_idesc(fmt, false, pa::kPfKeys);
+  a.idesc_pv = make_idesc(fmt, true, head_dim);
   a.err_flag = err_flag;
   a.num_chunks = num_chunks;
   a.qtiles = (int)qtiles;
@@ -952,16 +956,18 @@ int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_
                                num_blocks, scale, dtype, err_flag, a, tm_q, tm_k, tm_v, empty);
   if (st != PA_OK || empty) return st;
 
-  auto kern = dtype == PA_BF16 ? pa::prefill_kernel<__nv_bfloat16> : pa::prefill_kernel<__half>;
-  const int fmt = dtype == PA_BF16 ? 1 : 0;
+  auto kern = head_dim == 128
+                  ? (dtype == PA_BF16 ? pa::prefill_kernel<__nv_bfloat16, 128> : pa::prefill_kernel<__half, 128>)
+                  : (dtype == PA_BF16 ? pa::prefill_kernel<__nv_bfloat16, 64> : pa::prefill_kernel<__half, 64>);
+  const int variant = (dtype == PA_BF16 ? 1 : 0) + (head_dim == 128 ? 2 : 0);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
-  static int configured[2][64] = {{0}};
-  if (!configured[fmt][dev]) {
+  static int configured[4][64] = {{0}};
+  if (!configured[variant][dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pa::kPfSmemBytes) !=
         cudaSuccess)
       return PA_ERR_CUDA;
-    configured[fmt][dev] = 1;
+    configured[variant][dev] = 1;
   }
   const long long n_items = (long long)a.qtiles * num_chunks * num_heads;
   const int sms = device_sm_count();

@@ -175,3 +175,16 @@ def test_mixed_step_with_one_part_empty(pa):
     assert pa.pa_get_error(err) == 0
     assert torch.equal(d.view(torch.int16), ref_d.view(torch.int16))
     assert torch.equal(p.view(torch.int16), ref_p.view(torch.int16))
+
+
+def test_mixed_step_head_dim_64(pa):
+    m = W.mixed_prefill(device="cuda", num_decode=8, chunk_len=200, ctx_before=(300, 1000), D=64)
+    st = Step(pa, m)
+    w = m.decode
+    err = pa.new_error_flag()
+    pa.pa_reshape_and_cache(st.k_new, st.v_new, w.k_pool, w.v_pool, st.slots, err)
+    ref_d, ref_p = st.separate(pa, err)
+    d, p = st.mixed(pa, err)
+    assert pa.pa_get_error(err) == 0
+    assert torch.equal(d.view(torch.int16), ref_d.view(torch.int16))
+    assert torch.equal(p.view(torch.int16), ref_p.view(torch.int16))

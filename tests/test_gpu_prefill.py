@@ -141,3 +141,15 @@ def test_prefill_many_short_chunks(pa, n_chunks):
     assert flags == 0
     ref, _, _ = oracle_prefill(m)
     assert_attn_close(out, ref, "bf16", f"prefill {n_chunks} short chunks")
+
+
+@pytest.mark.parametrize("dtype,out_dtype,B", [("bf16", "f32", 16), ("f16", "f16", 256), ("bf16", "bf16", 48)])
+def test_prefill_head_dim_64(pa, dtype, out_dtype, B):
+    """head_dim 64: one swizzled 64-column half per tile, K = 64 for S and
+    N = 64 for P V; ragged chunks over several key tiles, one chunk at
+    context 0 (rows with one or two keys)."""
+    m = W.small_prefill(chunk_lens=(300, 77, 1), ctx_before=(150, 0, 700), H=3, D=64, B=B, dtype=dtype)
+    out, flags, _, _ = run_prefill(pa, m, out_dtype)
+    assert flags == 0
+    ref, _, _ = oracle_prefill(m)
+    assert_attn_close(out, ref, out_dtype, f"prefill head_dim 64 {dtype} block {B}")

@@ -199,6 +199,9 @@ WORKLOAD_TEXT = {
 MIXED = ("mixed", "budget512")
 WORKLOAD_TEXT["memsim"] = ("host-only memory simulator: seeded long-tailed and short request traces, KV capacity "
                            "32768 tokens, reservation baselines (first fit) vs paged blocks of 16")
+WORKLOAD_TEXT["prefix_cache"] = ("prefix caching: 16 requests = a shared 1024-token system prompt + 256 tokens of "
+                                 "their own, 40 heads x 128, block 16, bf16; suffix prefill over cached blocks vs "
+                                 "whole-prompt prefill")
 WORKLOAD_TEXT["swap"] = ("block swap: K/V of 8 requests x 2048 tokens, 40 heads x 128, fp16, block sizes 16..256, "
                          "GPU pool (blocks scattered) <-> pinned host pool")
 
@@ -754,6 +757,107 @@ def run_swap(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_prefix_cache(args, rank, world, local):
+    """Prefix caching on the GPU: 16 requests whose prompts share a
+    1024-token system prompt and end in 256 tokens of their own.  With the
+    allocator's prefix cache the prompt's 64 blocks are held once (filled by
+    an earlier request) and each step prefills only the 16 suffixes over
+    them (chunks of 256 queries at context 1024); without it every request
+    holds and prefills its whole 1280-token prompt.  Reports both prefill
+    times, the blocks held, and checks that the suffix rows agree bit for
+    bit."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_35_gb300 as pa
+    import pa_workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    n_req, shared, own, H, D, B = 16, 1024, 256, 40, 128, 16
+    L = shared + own
+    g = torch.Generator().manual_seed(7)
+    sys_ids = torch.randint(0, 32000, (shared,), generator=g).tolist()
+    prompts = [sys_ids + torch.randint(0, 32000, (own,), generator=g).tolist() for _ in range(n_req + 1)]
+    # K/V/q of a position depend on its whole prefix: equal for the shared prompt, drawn per request after it
+    kv_sys = [W.normal((shared, H, D), 300 + i, torch.bfloat16) for i in range(3)]
+    kv_own = [[W.normal((own, H, D), 1000 * (r + 1) + i, torch.bfloat16) for i in range(3)] for r in range(n_req + 1)]
+    full = lambda r, i: torch.cat([kv_sys[i], kv_own[r][i]])
+    err = pa.new_error_flag(dev)
+    scale = 1.0 / np.sqrt(D)
+
+    def build(cached: bool):
+        nb = (n_req + 1) * (L // B) + 8
+        alloc = pa.BlockAllocator(nb, B, prefix_cache=cached)
+        kp = torch.zeros(nb, H, B, D, dtype=torch.bfloat16, device=dev)
+        vp = torch.zeros_like(kp)
+        ks, vs, slots, first = [], [], [], []
+        for r in range(n_req + 1):  # request 0 fills the cache (when there is one)
+            n0 = alloc.add_seq_prefix(r, prompts[r])
+            first.append(n0)
+            for p_ in range(n0, L):
+                slots.append(int(alloc.append_tokens([r], [prompts[r][p_]])[0][0]))
+            ks.append(full(r, 0)[n0:])
+            vs.append(full(r, 1)[n0:])
+        pa.pa_reshape_and_cache(torch.cat(ks).to(dev), torch.cat(vs).to(dev), kp, vp,
+                                torch.tensor(slots, dtype=torch.int64, device=dev), err, stream)
+        reqs = list(range(1, n_req + 1))
+        mb = L // B
+        tables, _ = alloc.block_tables(reqs, mb)
+        c0 = [first[r] for r in reqs]
+        q = torch.cat([full(r, 2)[first[r]:] for r in reqs]).to(dev)
+        lens = [L - x for x in c0]
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+        out = torch.empty(q.shape[0], H, D, dtype=torch.bfloat16, device=dev)
+        cb = torch.tensor(c0, dtype=torch.int32, device=dev)
+        tb = torch.from_numpy(tables).to(dev)
+        held = nb - alloc.num_free()
+        fn = lambda: pa.pa_prefill_chunk(out, q, cu, cb, kp, vp, tb, max(lens), scale, err, stream)
+        flops = sum(4 * D * H * sum(x + i + 1 for i in range(L - x)) for x in c0)
+        alloc.close()
+        return fn, out, lens, held, flops, c0
+
+    res = {}
+    outs = {}
+    for cached in (True, False):
+        fn, out, lens, held, flops, c0 = build(cached)
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        K = max(5, min(args.steps, 200))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / K
+        key = "cached" if cached else "uncached"
+        res[key] = {"prefill_us": ms * 1e3, "queries": sum(lens), "context_before": c0[0], "gflop": flops / 1e9,
+                    "tflops": flops / (ms / 1e3) / 1e12, "blocks_held": held}
+        outs[key] = (out, lens)
+    if pa.pa_get_error(err, stream):
+        raise RuntimeError("device error flags in the prefix-cache workload")
+    # the suffix rows of the uncached prefill must equal the cached prefill's rows
+    oc, _ = outs["cached"]
+    ou, lu = outs["uncached"]
+    rows = torch.cat([torch.arange(sum(lu[:i]) + shared, sum(lu[:i + 1])) for i in range(n_req)]).to(dev)
+    same = bool(torch.equal(ou[rows].view(torch.int16), oc.view(torch.int16)))
+    if not same:
+        raise RuntimeError("cached and uncached prefill rows differ")
+    speed = res["uncached"]["prefill_us"] / res["cached"]["prefill_us"]
+    line = {"metric": "prefill time with a cached shared prompt, relative to prefilling whole prompts", "value": speed,
+            "unit": "x", "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT["prefix_cache"], "parallelism": f"replicas x{world}"},
+            "cached": res["cached"], "uncached": res["uncached"],
+            "memory_saving": 1.0 - res["cached"]["blocks_held"] / res["uncached"]["blocks_held"],
+            "suffix_rows_bit_identical": same, "gpu_launches": K}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_memsim(args, rank, world):
     """Host-only: KV memory holding tokens under Orca-Max / Orca-Pow2 /
     Orca-Oracle reservations and under the paged allocator, on two seeded
@@ -799,6 +903,8 @@ def main():
     rank, world, local = dist_setup()
     if args.workload == "swap":
         run_swap(args, rank, world, local)
+    elif args.workload == "prefix_cache":
+        run_prefix_cache(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -14,9 +14,10 @@
 //              [token][head][dim]) once the previous item's last S = Q K^T is
 //              done with the buffer; per 128-key tile the K rows and the V
 //              rows of its pages into 2- and 3-stage rings (2-D tensor maps
-//              over the pool seen as [block*H*B + slot][dim]); pages outside
-//              the table are read at an out-of-range row, which the TMA fills
-//              with zeros;
+//              over the pool seen as [block*H*B + slot][dim]), one lane per
+//              page piece issuing that piece's copies, its table entry read a
+//              tile ahead; pages outside the table are read at an
+//              out-of-range row, which the TMA fills with zeros;
 //      warp 8  (MMA)     one thread issues tcgen05.mma (kind::f16, M = N = 128,
 //              K = 16, fp32 accumulators in tensor memory): S(j) = Q K_j^T
 //              into one of two score buffers, and for each half h of the key
@@ -471,20 +472,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       if (!__shfl_sync(0xffffffffu, wok, 0)) break;
-      int prev_row = 0;  // this lane's page row of the previous key tile (its V is loaded one step later)
+      // Lane i < loads owns page piece i of every key tile: it looks up the
+      // piece's table entry one tile ahead and issues the piece's copies
+      // itself, so the pieces of a tile go out in parallel.
+      const bool owner = lane < loads;
+      auto fetch = [&](int t) -> int32_t {  // table entry of this lane's piece of tile t; -2: past the context
+        const int pos = t * kPfKeys + lane * rpl;
+        return (owner && t < it.n_kv && pos < it.ctx_total) ? __ldg(trow + pos / B) : -2;
+      };
+      int32_t entry = fetch(0);
+      int prev_row = a.pool_rows;  // this lane's page row of the previous key tile (its V is loaded one step later)
       for (int t = 0; t <= it.n_kv; ++t) {
         int row = a.pool_rows;  // out of range: the TMA fills zeros
-        if (t < it.n_kv && lane < loads) {
+        if (entry != -2) {
           const int pos = t * kPfKeys + lane * rpl;
-          if (pos < it.ctx_total) {
-            const int32_t blk = __ldg(trow + pos / B);
-            if (blk >= 0 && blk < a.num_blocks) {
-              row = (blk * H + it.h) * B + pos % B;
-            } else {
-              atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
-            }
+          if (entry >= 0 && entry < a.num_blocks) {
+            row = (entry * H + it.h) * B + pos % B;
+          } else {
+            atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
           }
         }
+        entry = fetch(t + 1);
         int wk = 1;
         if (t < it.n_kv) {  // K of tile t
           const int x = g + t;
@@ -495,13 +503,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             break;
           }
           if (lane == 0) mbar_arrive_expect_tx(&bars.k_full[stg], kLoadBytes);
-          for (int pc = 0; pc < loads; ++pc) {
-            const int rr = __shfl_sync(0xffffffffu, row, pc);
-            if (lane == 0) {
-              const uint32_t dst = base + kOffK + stg * kTileBytes + (uint32_t)pc * rpl * 128u;
-              tma_load_2d(dst, &tm_k, 0, rr, &bars.k_full[stg]);
-              if (kHalves == 2) tma_load_2d(dst + kHalfBytes, &tm_k, 64, rr, &bars.k_full[stg]);
-            }
+          __syncwarp();
+          if (owner) {
+            const uint32_t dst = base + kOffK + stg * kTileBytes + (uint32_t)lane * rpl * 128u;
+            tma_load_2d(dst, &tm_k, 0, row, &bars.k_full[stg]);
+            if (kHalves == 2) tma_load_2d(dst + kHalfBytes, &tm_k, 64, row, &bars.k_full[stg]);
           }
           ++k_issued;
         }
@@ -514,13 +520,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             break;
           }
           if (lane == 0) mbar_arrive_expect_tx(&bars.v_full[stg], kLoadBytes);
-          for (int pc = 0; pc < loads; ++pc) {
-            const int rr = __shfl_sync(0xffffffffu, prev_row, pc);
-            if (lane == 0) {
-              const uint32_t dst = base + kOffV + stg * kTileBytes + (uint32_t)pc * rpl * 128u;
-              tma_load_2d(dst, &tm_v, 0, rr, &bars.v_full[stg]);
-              if (kHalves == 2) tma_load_2d(dst + kHalfBytes, &tm_v, 64, rr, &bars.v_full[stg]);
-            }
+          __syncwarp();
+          if (owner) {
+            const uint32_t dst = base + kOffV + stg * kTileBytes + (uint32_t)lane * rpl * 128u;
+            tma_load_2d(dst, &tm_v, 0, prev_row, &bars.v_full[stg]);
+            if (kHalves == 2) tma_load_2d(dst + kHalfBytes, &tm_v, 64, prev_row, &bars.v_full[stg]);
           }
           ++v_issued;
         }

@@ -87,6 +87,9 @@ int pa_device_sm_count(void);
  * slot_mapping: device int64 [num_tokens].  Slots must be distinct (else the
  * result for the repeated slot is one of the writers).  A slot >= num_blocks*B
  * sets PA_FLAG_BAD_SLOT and that token is skipped.  num_tokens == 0 is a no-op.
+ * A kernel launched behind it with programmatic stream serialization may
+ * start while it runs and must wait (griddepcontrol.wait) before reading the
+ * pools.
  */
 int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                          const int64_t* slot_mapping, int num_tokens, int num_heads, int head_dim,
@@ -171,8 +174,12 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
  * partition_size: 0 = automatic, else a multiple of 16 in [16, 1024].
  * A table entry outside [0, num_blocks) sets PA_FLAG_BAD_BLOCK; the 16-token
  * chunk it covers is left out of that sequence's sum.
- * Launches: a one-CTA planning kernel, then the persistent decode kernel
- * (programmatic dependent launch) on `stream`.
+ * Launches: a one-CTA planning kernel, then the persistent decode kernel, on
+ * `stream`, each a programmatic dependent of the kernel before it: the
+ * planning (which reads only context_lens and writes only out rows of empty
+ * sequences and the workspace) may overlap a previous kernel that releases
+ * its dependents early, and completes only after that kernel has; the decode
+ * kernel waits for the planning kernel before reading anything.
  */
 int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,

@@ -19,6 +19,9 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
                                                                 const int64_t* __restrict__ slot_mapping,
                                                                 int64_t total_vecs, int vecs_per_head, int num_heads,
                                                                 int block_size, int64_t num_slots, int32_t* err_flag) {
+  // a kernel launched behind this one as a programmatic dependent (pa_decode's
+  // planning kernel) may start at once; it waits for this one before it ends
+  griddep_launch_dependents();
   const int64_t vecs_per_token = (int64_t)vecs_per_head * num_heads;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total_vecs;
        i += (int64_t)gridDim.x * blockDim.x) {

@@ -185,6 +185,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
     const int bkt = (last + kChunk - 1) / kChunk - 1;
     a.items[offs[bkt] + atomicAdd(&cur[bkt], 1)] = make_int4(s, nfull, nfull * P, last | (nparts << 11));
   }
+  // Launched as a programmatic dependent of the kernel before it (which may
+  // still be running, e.g. the slot scatter writing the pool): finish only
+  // after it has, so that the decode kernel's wait on this kernel also
+  // covers it.  The planning itself reads only the context lengths, which
+  // kernels that release their dependents early do not write.
+  griddep_wait();
 }
 
 // ---------------------------------------------------------------------------------
@@ -610,11 +616,21 @@ int configure_decode(int* occ_out) {
   return PA_OK;
 }
 
+// The planning kernel, as a programmatic dependent of the kernel before it.
 template <int D>
 int launch_plan(const pa::DecodeArgs& a, cudaStream_t stream) {
   const int nb = a.partition_size / pa::kChunk;
-  pa::plan_kernel<D><<<1, pa::kPlanThreads, 3 * nb * sizeof(int), stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(pa::kPlanThreads);
+  cfg.dynamicSmemBytes = 3 * nb * sizeof(int);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa::plan_kernel<D>, a) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 // The persistent decode kernel, launched as a programmatic dependent of the

@@ -319,6 +319,33 @@ int pa_decode_graphs_count(const pa_decode_graphs* g); /* graphs recorded so far
 void pa_decode_graphs_destroy(pa_decode_graphs* g);
 
 /*
+ * Host-side validation of the inputs the kernels index with (a debug aid).
+ * The kernels never trap on a bad block-table entry or length: they set a
+ * PA_FLAG_* bit and skip the work.  These calls find the first bad entry
+ * instead: they copy the tables and lengths to the host, SYNCHRONISE `stream`,
+ * and check exactly the entries the kernels would read (the ceil(len / B)
+ * entries of each row; [summary] section 4 block mapping).
+ *  - decode: context_lens[s] in [0, max_context_len] and <= max_blocks_per_seq
+ *    * block_size; entries 0 .. ceil(len/B)-1 of row s in [0, num_blocks).
+ *  - prefill: cu_q_lens[0] == 0, cu_q_lens[num_chunks] == total_q, chunk
+ *    lengths in [0, max_q_len], ctx_before[c] >= 0, ctx_before[c] + length
+ *    within the table row, entries covering it in [0, num_blocks).
+ * Return PA_OK or PA_ERR_BAD_INDEX; bad_out (int64[2], may be NULL) receives
+ * (row, logical block) of the first bad entry, logical block -1 for a bad
+ * length, (-1, -1) for bad cu_q_lens ends or when all is well.
+ * With the environment variable PA_DEBUG set (not "0"), pa_decode,
+ * pa_prefill_chunk and pa_mixed_step run these checks before launching and
+ * return PA_ERR_BAD_INDEX (nothing launched, a line on stderr) on a bad entry.
+ * Every GPU entry point also opens an NVTX range named after itself.
+ */
+int pa_check_decode_inputs(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                           int num_seqs, int max_context_len, int block_size, int num_blocks, void* stream,
+                           int64_t* bad_out);
+int pa_check_prefill_inputs(const int32_t* cu_q_lens, const int32_t* ctx_before, const int32_t* block_tables,
+                            int max_blocks_per_seq, int num_chunks, int total_q, int max_q_len, int block_size,
+                            int num_blocks, void* stream, int64_t* bad_out);
+
+/*
  * pa_get_error -- synchronise `stream`, read the device error flag, clear it.
  * Returns PA_OK, PA_ERR_TIMEOUT (if PA_FLAG_TIMEOUT is set), PA_ERR_BAD_INDEX
  * (any other flag) or PA_ERR_CUDA.  If flags_out is non-null it receives the

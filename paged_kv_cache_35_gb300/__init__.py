@@ -63,6 +63,8 @@ SIGNATURES = {
     "pa_decode_graphs_run": ([_P, _I, _I, _P], _I),
     "pa_decode_graphs_count": ([_P], _I),
     "pa_decode_graphs_destroy": ([_P], None),
+    "pa_check_decode_inputs": ([_P, _I, _P, _I, _I, _I, _I, _P, _P], _I),
+    "pa_check_prefill_inputs": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "pa_get_error": ([_P, _P, _P], _I),
     "pa_slot_mapping": ([_P, _I, _I, _I, _P, _P, _I, _P], _I),
     "pa_alloc_create": ([_I, _I, _P], _I),
@@ -314,6 +316,39 @@ def pa_mixed_step(dec_out, dec_q, dec_block_tables, context_lens, max_context_le
         H, D, B, NB, float(scale), _kv_code(k_pool), int(prefill_sms), _dev(err_flag, "err_flag", torch.int32),
         _stream(stream))
     _check(st, "pa_mixed_step")
+
+
+def pa_check_decode_inputs(block_tables, context_lens, max_context_len, block_size, num_blocks, stream=None):
+    """Host-side check of a decode's tables and lengths (synchronises the
+    stream).  Returns None, or (sequence, logical block) of the first bad
+    entry (logical block -1: a bad length)."""
+    S = context_lens.shape[0]
+    bad = np.zeros(2, dtype=np.int64)
+    st = lib().pa_check_decode_inputs(_dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                                      _dev(context_lens, "context_lens", torch.int32), S, int(max_context_len),
+                                      int(block_size), int(num_blocks), _stream(stream), bad.ctypes.data)
+    if st == PA_ERR_BAD_INDEX:
+        return int(bad[0]), int(bad[1])
+    _check(st, "pa_check_decode_inputs")
+    return None
+
+
+def pa_check_prefill_inputs(cu_q_lens, ctx_before, block_tables, total_q, max_q_len, block_size, num_blocks,
+                            stream=None):
+    """Host-side check of a prefill's chunk bounds and tables (synchronises
+    the stream).  Returns None, or (chunk, logical block) of the first bad
+    entry (logical block -1: a bad length; (-1, -1): bad cu_q_lens ends)."""
+    C = ctx_before.shape[0]
+    bad = np.zeros(2, dtype=np.int64)
+    st = lib().pa_check_prefill_inputs(_dev(cu_q_lens, "cu_q_lens", torch.int32),
+                                       _dev(ctx_before, "ctx_before", torch.int32),
+                                       _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1], C,
+                                       int(total_q), int(max_q_len), int(block_size), int(num_blocks),
+                                       _stream(stream), bad.ctypes.data)
+    if st == PA_ERR_BAD_INDEX:
+        return int(bad[0]), int(bad[1])
+    _check(st, "pa_check_prefill_inputs")
+    return None
 
 
 def pa_get_error(err_flag, stream=None) -> int:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libpa.so")
 
-CU_SOURCES = ["pa_cache_ops.cu", "pa_decode.cu", "pa_prefill.cu", "pa_graph.cu"]
+CU_SOURCES = ["pa_cache_ops.cu", "pa_decode.cu", "pa_prefill.cu", "pa_graph.cu", "pa_checks.cu"]
 CPP_SOURCES = ["pa_allocator.cpp"]
 HEADERS = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))] + [
     os.path.join(ROOT, "include", "pa.h")

@@ -153,6 +153,7 @@ int pa_device_sm_count(void) { return pa_host::device_sm_count(); }
 int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                          const int64_t* slot_mapping, int num_tokens, int num_heads, int head_dim, int block_size,
                          int num_blocks, int dtype, int32_t* err_flag, void* stream) {
+  pa_host::Range range("pa_reshape_and_cache");
   if (num_tokens < 0 || num_heads <= 0 || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
   if (!pa_host::is_kv_dtype(dtype)) return PA_ERR_UNSUPPORTED;
   if (head_dim <= 0 || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
@@ -176,6 +177,7 @@ int pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_pool, voi
 
 int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int n_pairs, int num_heads, int head_dim,
                    int block_size, int num_blocks, int dtype, int32_t* err_flag, void* stream) {
+  pa_host::Range range("pa_copy_blocks");
   if (n_pairs < 0 || num_heads <= 0 || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
   if (!pa_host::is_kv_dtype(dtype)) return PA_ERR_UNSUPPORTED;
   if (head_dim <= 0 || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
@@ -196,6 +198,7 @@ int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int n_pairs
 int pa_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks, void* dst_k, void* dst_v,
                    int dst_num_blocks, const int32_t* pairs, int n_pairs, int num_heads, int head_dim,
                    int block_size, int dtype, int32_t* err_flag, void* stream) {
+  pa_host::Range range("pa_swap_blocks");
   if (n_pairs < 0 || num_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_size <= 0)
     return PA_ERR_INVALID_ARG;
   if (!pa_host::is_kv_dtype(dtype)) return PA_ERR_UNSUPPORTED;
@@ -219,6 +222,7 @@ int pa_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks, voi
 }
 
 int pa_get_error(int32_t* err_flag, int32_t* flags_out, void* stream) {
+  pa_host::Range range("pa_get_error");
   if (err_flag == nullptr) return PA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   int32_t h = 0;

@@ -12,6 +12,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -165,6 +167,27 @@ inline bool is_out_dtype(int dtype) { return dtype == PA_F16 || dtype == PA_BF16
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int device_sm_count();
+
+// An NVTX range named after the C-ABI call, open for the call's host-side
+// duration (visible in Nsight timelines; costs nothing measurable without a
+// tool attached).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+
+// True when the environment variable PA_DEBUG is set to a non-empty value
+// other than "0" (read once per process): the decode and prefill entry points
+// then validate their tables and lengths on the host before launching.
+bool debug_checks();
+int check_decode_inputs(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                        int num_seqs, int max_context_len, int block_size, int num_blocks, void* stream,
+                        int64_t* bad_out);
+int check_prefill_inputs(const int32_t* cu_q_lens, const int32_t* ctx_before, const int32_t* block_tables,
+                         int max_blocks_per_seq, int num_chunks, int total_q, int max_q_len, int block_size,
+                         int num_blocks, void* stream, int64_t* bad_out);
 
 // Argument checks of pa_decode / pa_prefill_chunk that launch nothing, and
 // the prefill launch with its persistent grid capped at max_ctas CTAs

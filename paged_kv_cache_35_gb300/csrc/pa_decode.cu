@@ -46,6 +46,8 @@
 
 #include <mutex>
 
+#include <cstdio>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -781,12 +783,23 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
               int num_seqs, int num_heads, int head_dim, int block_size, int num_blocks, float scale, int dtype,
               void* workspace, size_t workspace_bytes, int partition_size, int32_t* err_flag, void* stream) {
+  pa_host::Range range("pa_decode");
   pa::DecodeArgs a;
   bool empty = false;
-  const int st = decode_setup(out, out_dtype, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
-                              max_context_len, num_seqs, num_heads, head_dim, block_size, num_blocks, scale, dtype,
-                              workspace, workspace_bytes, partition_size, err_flag, a, empty);
+  int st = decode_setup(out, out_dtype, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                        max_context_len, num_seqs, num_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
+                        workspace_bytes, partition_size, err_flag, a, empty);
   if (st != PA_OK || empty) return st;
+  if (pa_host::debug_checks()) {
+    int64_t bad[2];
+    st = pa_host::check_decode_inputs(block_tables, max_blocks_per_seq, context_lens, num_seqs, max_context_len,
+                                      block_size, num_blocks, stream, bad);
+    if (st != PA_OK) {
+      std::fprintf(stderr, "pa_decode (PA_DEBUG): sequence %lld, logical block %lld is invalid\n", (long long)bad[0],
+                   (long long)bad[1]);
+      return st;
+    }
+  }
   cudaStream_t s = (cudaStream_t)stream;
   if (head_dim == 128) {
     return dtype == PA_F16 ? launch_decode<128, __half>(a, s) : launch_decode<128, __nv_bfloat16>(a, s);
@@ -812,6 +825,7 @@ int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int
                   int pf_max_blocks_per_seq, int num_chunks, int total_q, int max_q_len, const void* k_pool,
                   const void* v_pool, int num_heads, int head_dim, int block_size, int num_blocks, float scale,
                   int dtype, int prefill_sms, int32_t* err_flag, void* stream) {
+  pa_host::Range range("pa_mixed_step");
   pa::DecodeArgs a;
   bool dec_empty = false;
   int st = decode_setup(dec_out, dec_out_dtype, dec_q, k_pool, v_pool, dec_block_tables, dec_max_blocks_per_seq,
@@ -823,6 +837,26 @@ int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int
                               num_blocks, scale, dtype, err_flag);
   if (st != PA_OK) return st;
   const bool pf_empty = num_chunks == 0 || total_q == 0 || max_q_len == 0;
+  if (pa_host::debug_checks() && !dec_empty) {
+    int64_t bad[2];
+    st = pa_host::check_decode_inputs(dec_block_tables, dec_max_blocks_per_seq, context_lens, num_seqs,
+                                      max_context_len, block_size, num_blocks, stream, bad);
+    if (st != PA_OK) {
+      std::fprintf(stderr, "pa_mixed_step (PA_DEBUG): sequence %lld, logical block %lld is invalid\n",
+                   (long long)bad[0], (long long)bad[1]);
+      return st;
+    }
+  }
+  if (pa_host::debug_checks() && !pf_empty) {
+    int64_t bad[2];
+    st = pa_host::check_prefill_inputs(cu_q_lens, ctx_before, pf_block_tables, pf_max_blocks_per_seq, num_chunks,
+                                       total_q, max_q_len, block_size, num_blocks, stream, bad);
+    if (st != PA_OK) {
+      std::fprintf(stderr, "pa_mixed_step (PA_DEBUG): chunk %lld, logical block %lld is invalid\n",
+                   (long long)bad[0], (long long)bad[1]);
+      return st;
+    }
+  }
   const int sms = pa_host::device_sm_count();
   if (sms <= 0) return PA_ERR_CUDA;
   int cap = prefill_sms > 0 ? (prefill_sms < sms ? prefill_sms : sms) : (sms * PA_MIXED_PREFILL_SHARE + 50) / 100;
@@ -867,6 +901,7 @@ extern "C" int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
                                         const int32_t* context_lens, int max_context_len, int num_seqs,
                                         int num_heads, int head_dim, int block_size, int num_blocks, float scale,
                                         int dtype, int partition_size, int32_t* err_flag, void* stream) {
+  pa_host::Range range("pa_decode_static_scratch");
   const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size);
   if (need > (size_t)PA_DECODE_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
   int dev = 0;

@@ -141,6 +141,7 @@ void pa_decode_graphs_destroy(pa_decode_graphs* g) {
 int pa_decode_graphs_count(const pa_decode_graphs* g) { return g ? (int)g->graphs.size() : -1; }
 
 int pa_decode_graphs_run(pa_decode_graphs* g, int num_seqs, int max_context_len, void* stream) {
+  pa_host::Range range("pa_decode_graphs_run");
   if (g == nullptr || num_seqs < 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   const int s_pad = round_up(num_seqs, g->seq_interval);

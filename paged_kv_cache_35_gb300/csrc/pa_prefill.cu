@@ -57,6 +57,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <cstdio>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -955,10 +956,20 @@ int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_
   pa::PrefillArgs a;
   CUtensorMap tm_q, tm_k, tm_v;
   bool empty = false;
-  const int st = prefill_setup(out, out_dtype, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables,
-                               max_blocks_per_seq, num_chunks, total_q, max_q_len, num_heads, head_dim, block_size,
-                               num_blocks, scale, dtype, err_flag, a, tm_q, tm_k, tm_v, empty);
+  int st = prefill_setup(out, out_dtype, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables,
+                         max_blocks_per_seq, num_chunks, total_q, max_q_len, num_heads, head_dim, block_size,
+                         num_blocks, scale, dtype, err_flag, a, tm_q, tm_k, tm_v, empty);
   if (st != PA_OK || empty) return st;
+  if (debug_checks()) {
+    int64_t bad[2];
+    st = check_prefill_inputs(cu_q_lens, ctx_before, block_tables, max_blocks_per_seq, num_chunks, total_q,
+                              max_q_len, block_size, num_blocks, stream, bad);
+    if (st != PA_OK) {
+      std::fprintf(stderr, "pa_prefill_chunk (PA_DEBUG): chunk %lld, logical block %lld is invalid\n",
+                   (long long)bad[0], (long long)bad[1]);
+      return st;
+    }
+  }
 
   auto kern = head_dim == 128
                   ? (dtype == PA_BF16 ? pa::prefill_kernel<__nv_bfloat16, 128> : pa::prefill_kernel<__half, 128>)
@@ -990,6 +1001,7 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
                                 const int32_t* block_tables, int max_blocks_per_seq, int num_chunks, int total_q,
                                 int max_q_len, int num_heads, int head_dim, int block_size, int num_blocks,
                                 float scale, int dtype, int32_t* err_flag, void* stream) {
+  pa_host::Range range("pa_prefill_chunk");
   return pa_host::prefill_launch(out, out_dtype, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables,
                                  max_blocks_per_seq, num_chunks, total_q, max_q_len, num_heads, head_dim, block_size,
                                  num_blocks, scale, dtype, err_flag, 0, stream);

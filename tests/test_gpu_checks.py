@@ -1,0 +1,99 @@
+"""Host-side input validation (pa_check_decode_inputs /
+pa_check_prefill_inputs) and the PA_DEBUG mode that runs it before every
+decode and prefill launch."""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+import pa_workloads as W
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_35_gb300 as pa
+
+    torch.cuda.set_device(0)
+    return pa
+
+
+def test_decode_input_check_finds_the_first_bad_entry(pa):
+    w = W.small_decode(ctx=(1, 17, 300, 40), H=2, D=64)
+    B, NB, mx = w.block_size, w.num_blocks, int(w.context_lens.max())
+    tables, ctx = w.block_tables.clone(), w.context_lens.clone()
+    dev = torch.device("cuda")
+    assert pa.pa_check_decode_inputs(tables.to(dev), ctx.to(dev), mx, B, NB) is None
+    # an entry past a sequence's blocks is never read: not an error
+    t2 = tables.clone()
+    t2[0, -1] = 10 ** 6
+    assert pa.pa_check_decode_inputs(t2.to(dev), ctx.to(dev), mx, B, NB) is None
+    t2[2, 5] = -7  # sequence 2 (300 tokens) reads blocks 0..18
+    t2[3, 1] = NB  # sequence 3 (40 tokens) reads blocks 0..2
+    assert pa.pa_check_decode_inputs(t2.to(dev), ctx.to(dev), mx, B, NB) == (2, 5)
+    c2 = ctx.clone()
+    c2[1] = tables.shape[1] * B + 1  # longer than its table row
+    assert pa.pa_check_decode_inputs(tables.to(dev), c2.to(dev), 10 ** 6, B, NB) == (1, -1)
+    c2[1] = mx + 1  # past max_context_len
+    assert pa.pa_check_decode_inputs(tables.to(dev), c2.to(dev), mx, B, NB) == (1, -1)
+
+
+def test_prefill_input_check_finds_the_first_bad_entry(pa):
+    m = W.small_prefill(chunk_lens=(130, 77), ctx_before=(200, 37), H=2, B=16)
+    dev = torch.device("cuda")
+    cu = torch.tensor([0, 130, 207], dtype=torch.int32, device=dev)
+    cb = m.ctx_before.to(dev)
+    tb = m.chunk_tables.clone()
+    NB = m.decode.num_blocks
+    assert pa.pa_check_prefill_inputs(cu, cb, tb.to(dev), 207, 130, 16, NB) is None
+    tb[1, 4] = -1  # chunk 1 covers positions 0..113: blocks 0..7
+    assert pa.pa_check_prefill_inputs(cu, cb, tb.to(dev), 207, 130, 16, NB) == (1, 4)
+    assert pa.pa_check_prefill_inputs(cu, cb, m.chunk_tables.to(dev), 206, 130, 16, NB) == (-1, -1)
+    assert pa.pa_check_prefill_inputs(cu, cb, m.chunk_tables.to(dev), 207, 100, 16, NB) == (0, -1)
+
+
+SCRIPT = r"""
+import torch, pa_workloads as W
+import paged_kv_cache_35_gb300 as pa
+w = W.small_decode(ctx=(33, 300), H=2, D=64)
+dev = torch.device("cuda")
+t = w.block_tables.clone(); t[1, 3] = -4
+out = torch.zeros(2, 2, 64, dtype=torch.float16, device=dev)
+err = pa.new_error_flag()
+ws = pa.decode_workspace(2, 2, 64, 300)
+try:
+    pa.pa_decode(out, w.q.to(dev), w.k_pool.to(dev), w.v_pool.to(dev), t.to(dev), w.context_lens.to(dev), 300,
+                 w.scale, ws, err)
+    print("launched", pa.pa_get_error(err))
+except pa.PAError as e:
+    print("refused", e.status, pa.pa_get_error(err))
+"""
+
+
+def _run(env_value):
+    env = dict(os.environ)
+    env.pop("PA_DEBUG", None)
+    if env_value is not None:
+        env["PA_DEBUG"] = env_value
+    r = subprocess.run([sys.executable, "-c", SCRIPT], cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    return r.stdout.strip().splitlines()[-1], r.stderr
+
+
+def test_pa_debug_refuses_bad_tables_before_any_launch(pa):
+    import paged_kv_cache_35_gb300 as pa_mod
+
+    line, err_text = _run("1")
+    assert line == f"refused {pa_mod.PA_ERR_BAD_INDEX} 0", line  # nothing ran: the device flag is clear
+    assert "sequence 1, logical block 3" in err_text
+    line, _ = _run(None)  # without PA_DEBUG the kernel runs, skips the bad chunk and flags it
+    assert line == f"launched {pa_mod.PA_FLAG_BAD_BLOCK}", line

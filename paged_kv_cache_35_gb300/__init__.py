@@ -7,8 +7,13 @@ the library's CUDA kernels (or, for the block allocator, its host C++).
 There is no fallback: if ``libpa.so`` has not been built, every call raises.
 
 Names match the C entry points: ``pa_reshape_and_cache``, ``pa_copy_blocks``,
-``pa_decode``, ``pa_prefill_chunk``, ``pa_get_error``, ``pa_slot_mapping``,
-and the ``pa_alloc_*`` allocator (wrapped by :class:`BlockAllocator`).
+``pa_swap_blocks``, ``pa_decode``, ``pa_decode_static_scratch``,
+``pa_prefill_chunk``, ``pa_mixed_step``, ``pa_check_decode_inputs``,
+``pa_check_prefill_inputs``, ``pa_get_error``, ``pa_slot_mapping``; the
+``pa_decode_graphs_*`` graph cache is wrapped by :class:`DecodeGraphs` and the
+``pa_alloc_*`` allocator (with its optional prefix cache) by
+:class:`BlockAllocator`.  ``memsim`` is a host-only memory-waste simulator
+built on the allocator.
 """
 from __future__ import annotations
 

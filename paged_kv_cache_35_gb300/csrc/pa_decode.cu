@@ -41,12 +41,17 @@
 //  * Each CTA's first unit is its own index (no counter round trip at start);
 //    the work items carry their token count and partition count, so the
 //    scheduler's chain is counter -> item -> table entries.
+//  * Both kernels are programmatic dependents of the kernel before them: the
+//    planning kernel may overlap a slot scatter that releases it early and
+//    waits for it only at its end; the decode grid is resident while the
+//    planning runs and waits for it before reading anything.
+//  * pa_mixed_step (end of this file) puts the chunked prefill between the
+//    planning kernel and the decode kernel so that the two run concurrently.
 //  * Every wait is bounded; bad table entries are flagged, never trapped.
 #include <math.h>
 
-#include <mutex>
-
 #include <cstdio>
+#include <mutex>
 
 #include "pa_common.cuh"
 

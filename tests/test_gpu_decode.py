@@ -142,9 +142,9 @@ def test_decode_partition_sizes_agree(pa, P):
     assert_attn_close(out, oracle_decode(w), "f32", f"partition {P}")
 
 
-@pytest.mark.parametrize("B", [16, 32, 256])
+@pytest.mark.parametrize("B", [16, 32, 48, 256, 1024, 4096])
 def test_decode_block_sizes(pa, B):
-    w = W.small_decode(ctx=(1, 31, 300, 777), H=2, B=B, dtype="f16")
+    w = W.small_decode(ctx=(1, 31, 300, 777, 5000), H=2, B=B, dtype="f16")
     out, flags = run_decode(pa, w, out_dtype="f32")
     assert flags == 0
     assert_attn_close(out, oracle_decode(w), "f32", f"block {B}")

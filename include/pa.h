@@ -346,6 +346,18 @@ int pa_check_prefill_inputs(const int32_t* cu_q_lens, const int32_t* ctx_before,
                             int num_blocks, void* stream, int64_t* bad_out);
 
 /*
+ * pa_selftest_wait_timeout -- exercises the bounded wait every kernel uses;
+ * the paper has no counterpart.  One CTA copies 4 KiB from `src` (device,
+ * 16-byte aligned) into shared memory with a bulk copy, then waits on an
+ * mbarrier that nothing arrives at.  After the kernels' wait limit (1 s) the
+ * wait gives up and sets PA_FLAG_TIMEOUT in *err_flag; the CTA then lets its
+ * own copy land and exits normally, leaving the context usable.  result
+ * (device int32[3]) receives: the wait's success (0 expected), whether the
+ * copy landed (1), and the copy's last 32-bit word.
+ */
+int pa_selftest_wait_timeout(const void* src, int32_t* err_flag, int32_t* result, void* stream);
+
+/*
  * pa_get_error -- synchronise `stream`, read the device error flag, clear it.
  * Returns PA_OK, PA_ERR_TIMEOUT (if PA_FLAG_TIMEOUT is set), PA_ERR_BAD_INDEX
  * (any other flag) or PA_ERR_CUDA.  If flags_out is non-null it receives the

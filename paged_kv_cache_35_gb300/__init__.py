@@ -70,6 +70,7 @@ SIGNATURES = {
     "pa_decode_graphs_destroy": ([_P], None),
     "pa_check_decode_inputs": ([_P, _I, _P, _I, _I, _I, _I, _P, _P], _I),
     "pa_check_prefill_inputs": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pa_selftest_wait_timeout": ([_P, _P, _P, _P], _I),
     "pa_get_error": ([_P, _P, _P], _I),
     "pa_slot_mapping": ([_P, _I, _I, _I, _P, _P, _I, _P], _I),
     "pa_alloc_create": ([_I, _I, _P], _I),

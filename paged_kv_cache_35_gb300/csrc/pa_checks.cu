@@ -1,4 +1,5 @@
-// Host-side validation of block tables and lengths (debug aid).
+// Host-side validation of block tables and lengths (debug aid), and a
+// self-test of the kernels' bounded waits.
 //
 // The kernels never trap: a table entry outside the pool or a length past a
 // table only sets a bit in the device error flag and the bad work is skipped.
@@ -33,6 +34,37 @@ void report(int64_t* bad_out, int64_t row, int64_t logical_block) {
 }
 
 }  // namespace
+
+namespace pa {
+
+// Self-test of the bounded waits every kernel uses: one CTA puts a bulk copy
+// in flight on barrier `landed`, then waits on barrier `never`, which nothing
+// arrives at.  After the wait limit the wait sets PA_FLAG_TIMEOUT and gives
+// up; the CTA then waits (bounded, ignoring the abort) for its own copy to
+// land before it exits, as every kernel does on an abort.
+__global__ void selftest_wait_kernel(const uint4* __restrict__ src, int32_t* err_flag, int32_t* result) {
+  __shared__ __align__(128) uint4 buf[256];  // 4 KiB
+  __shared__ uint64_t landed, never;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&landed, 1);
+    mbar_init(&never, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&landed, sizeof(buf));
+    bulk_g2s(buf, src, sizeof(buf), &landed);
+    const bool ok = mbar_wait(&never, 0, &abort_flag, err_flag);
+    const bool drained = mbar_wait_drain(&landed, 0);
+    result[0] = ok ? 1 : 0;
+    result[1] = drained ? 1 : 0;
+    result[2] = drained ? (int32_t)buf[255].w : -1;
+  }
+}
+
+}  // namespace pa
 
 namespace pa_host {
 
@@ -124,6 +156,13 @@ int pa_check_prefill_inputs(const int32_t* cu_q_lens, const int32_t* ctx_before,
   pa_host::Range r("pa_check_prefill_inputs");
   return pa_host::check_prefill_inputs(cu_q_lens, ctx_before, block_tables, max_blocks_per_seq, num_chunks, total_q,
                                        max_q_len, block_size, num_blocks, stream, bad_out);
+}
+
+int pa_selftest_wait_timeout(const void* src, int32_t* err_flag, int32_t* result, void* stream) {
+  pa_host::Range r("pa_selftest_wait_timeout");
+  if (src == nullptr || err_flag == nullptr || result == nullptr || !pa_host::aligned16(src)) return PA_ERR_INVALID_ARG;
+  pa::selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(static_cast<const uint4*>(src), err_flag, result);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -97,3 +97,27 @@ def test_pa_debug_refuses_bad_tables_before_any_launch(pa):
     assert "sequence 1, logical block 3" in err_text
     line, _ = _run(None)  # without PA_DEBUG the kernel runs, skips the bad chunk and flags it
     assert line == f"launched {pa_mod.PA_FLAG_BAD_BLOCK}", line
+
+
+def test_a_wait_that_runs_out_flags_timeout_and_the_context_stays_usable(pa):
+    """A kernel waits, with the library's bounded wait, on an mbarrier that
+    nothing arrives at: after the limit it sets PA_FLAG_TIMEOUT, lets its
+    own bulk copy land and exits; then an ordinary decode runs correctly."""
+    import ctypes
+
+    dev = torch.device("cuda")
+    src = torch.arange(1024, dtype=torch.int32, device=dev)  # 4 KiB
+    err = pa.new_error_flag()
+    result = torch.full((3,), -2, dtype=torch.int32, device=dev)
+    st = pa.lib().pa_selftest_wait_timeout(src.data_ptr(), err.data_ptr(), result.data_ptr(),
+                                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == pa.PA_OK
+    assert pa.pa_get_error(err) == pa.PA_FLAG_TIMEOUT
+    assert result.tolist() == [0, 1, 1023]
+    w = W.small_decode(ctx=(5, 300), H=2, D=64)
+    out = torch.empty(2, 2, 64, dtype=torch.float32, device=dev)
+    ws = pa.decode_workspace(2, 2, 64, 300)
+    pa.pa_decode(out, w.q.to(dev), w.k_pool.to(dev), w.v_pool.to(dev), w.block_tables.to(dev),
+                 w.context_lens.to(dev), 300, w.scale, ws, err)
+    assert pa.pa_get_error(err) == 0
+    assert torch.isfinite(out).all()

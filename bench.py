@@ -199,6 +199,8 @@ WORKLOAD_TEXT = {
 MIXED = ("mixed", "budget512")
 WORKLOAD_TEXT["memsim"] = ("host-only memory simulator: seeded long-tailed and short request traces, KV capacity "
                            "32768 tokens, reservation baselines (first fit) vs paged blocks of 16")
+WORKLOAD_TEXT["batch_sweep"] = ("decode latency vs batch size 1..256, contexts of 1024, 40 heads x 128, fp16: "
+                                "16-token pages at random places vs one contiguous 1024-token block per sequence")
 WORKLOAD_TEXT["prefix_cache"] = ("prefix caching: 16 requests = a shared 1024-token system prompt + 256 tokens of "
                                  "their own, 40 heads x 128, block 16, bf16; suffix prefill over cached blocks vs "
                                  "whole-prompt prefill")
@@ -865,6 +867,75 @@ def run_prefix_cache(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_batch_sweep(args, rank, world, local):
+    """Decode latency against batch size, paged against contiguous: every
+    sequence has 1024 tokens, 40 heads x 128, fp16.  "paged": 16-token
+    blocks at random places in the pool; "contiguous": one 1024-token block
+    per sequence, the sequences' blocks in order (the K/V of a (sequence,
+    head) is one contiguous run, as without paging).  Same kernel, same
+    arithmetic; the difference is the cost of paging."""
+    import statistics
+
+    import torch
+
+    import paged_kv_cache_35_gb300 as pa
+    import pa_workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    H, D, ctx_len = 40, 128, 1024
+    rows = []
+    for S in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+        ctx = torch.full((S,), ctx_len, dtype=torch.int32)
+        w = W._decode_workload("batch_sweep_paged", ctx, ctx - 1, H, D, 16, "f16", device=dev)
+        tables = w.block_tables.to(dev)
+        lens = w.context_lens.to(dev)
+        # the same K/V, gathered per sequence in logical order: [S][H][ctx_len][D]
+        pos = torch.arange(ctx_len, device=dev)
+        blk = tables[:, pos // 16].long()  # [S][ctx_len]
+        gather = lambda pool: pool[blk, :, (pos % 16).expand(S, ctx_len), :].permute(0, 2, 1, 3).contiguous()
+        k_c, v_c = gather(w.k_pool), gather(w.v_pool)
+        t_c = torch.arange(S, dtype=torch.int32, device=dev).reshape(S, 1)
+        res = {"batch": S}
+        outs = {}
+        for kind, kp, vp, tb, B in (("paged", w.k_pool, w.v_pool, tables, 16), ("contiguous", k_c, v_c, t_c, ctx_len)):
+            out = torch.empty(S, H, D, dtype=torch.float16, device=dev)
+            ws = pa.decode_workspace(S, H, D, ctx_len, device=dev)
+            err = pa.new_error_flag(dev)
+            fn = lambda: pa.pa_decode(out, w.q, kp, vp, tb, lens, ctx_len, w.scale, ws, err, stream=stream)
+            for _ in range(10):
+                fn()
+            torch.cuda.synchronize(dev)
+            ts = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(50):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                ts.append(a.elapsed_time(b) / 50 * 1e3)
+            if pa.pa_get_error(err, stream):
+                raise RuntimeError("device error flags in the batch sweep")
+            us = statistics.median(ts)
+            res[kind + "_us"] = us
+            res[kind + "_GBs"] = decode_bytes([ctx_len] * S, H, D, B, 2) / us / 1e3
+            outs[kind] = out
+        res["bit_identical"] = bool(torch.equal(outs["paged"].view(torch.int16), outs["contiguous"].view(torch.int16)))
+        res["paged_over_contiguous"] = res["paged_us"] / res["contiguous_us"]
+        rows.append(res)
+        del w, k_c, v_c
+    worst = max(r["paged_over_contiguous"] for r in rows)
+    line = {"metric": "decode latency, 16-token pages relative to contiguous K/V (worst over batch sizes)",
+            "value": worst, "unit": "x", "n_gpus": world, "steps": 250, "warmup": 10, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT["batch_sweep"], "parallelism": f"replicas x{world}"},
+            "sweep": rows, "gpu_launches": 2 * 250 * len(rows) * 2}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_memsim(args, rank, world):
     """Host-only: KV memory holding tokens under Orca-Max / Orca-Pow2 /
     Orca-Oracle reservations and under the paged allocator, on two seeded
@@ -912,6 +983,8 @@ def main():
         run_swap(args, rank, world, local)
     elif args.workload == "prefix_cache":
         run_prefix_cache(args, rank, world, local)
+    elif args.workload == "batch_sweep":
+        run_batch_sweep(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

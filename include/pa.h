@@ -142,8 +142,12 @@ int pa_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks, voi
 
 /*
  * Split-KV partition length (tokens) that pa_decode uses when called with
- * partition_size == 0: a multiple of 16 between 64 and 1024, chosen from the
- * batch shape alone (no device query).
+ * partition_size == 0, chosen from the batch shape alone (no device query):
+ * with pairs = num_seqs * num_heads and units(P) = pairs *
+ * ceil(max_context_len / P), it is 1024 when pairs >= 380 and either
+ * max_context_len <= 1024 or units(1024) >= 12160 (16 waves of a 152-SM x
+ * 5-CTA grid); otherwise the largest of 512, 256, 128 with units(P) >= 380
+ * (half a wave), else 64.  512 when an argument is not positive.
  */
 int pa_decode_partition_size(int num_seqs, int num_heads, int max_context_len);
 

@@ -768,10 +768,21 @@ int decode_check(void* out, int out_dtype, const void* q, const void* k_pool, co
 
 extern "C" {
 
+// Partition length from the batch shape, for the 760-CTA grid (152 SMs x 5),
+// every sequence counted at the longest context:
+//  * 1024 when every context fits one partition and the (sequence, head)
+//    pairs alone give half a wave: no partials and no merge at all;
+//  * 1024 when even 1024-token units make 16 waves or more, so the tail of
+//    the longer units is negligible;
+//  * otherwise the longest of 512, 256, 128, 64 that gives half a wave of
+//    units (64 if none does).  With a few waves of ragged contexts, 1024-token
+//    units leave a longer tail than 512-token ones.
 int pa_decode_partition_size(int num_seqs, int num_heads, int max_context_len) {
   if (num_seqs <= 0 || num_heads <= 0 || max_context_len <= 0) return 512;
+  const long long pairs = (long long)num_seqs * num_heads;
+  if (pairs >= 380 && (max_context_len <= 1024 || pairs * ((max_context_len + 1023) / 1024) >= 16 * 760)) return 1024;
   int P = 512;
-  while (P > 64 && (long long)num_seqs * num_heads * ((max_context_len + P - 1) / P) < 1216) P /= 2;
+  while (P > 64 && pairs * ((max_context_len + P - 1) / P) < 380) P /= 2;
   return P;
 }
 

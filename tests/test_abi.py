@@ -93,10 +93,19 @@ def test_bad_arguments_are_rejected_before_launch(pa):
 
 
 def test_partition_and_workspace_sizes(pa):
-    assert pa.pa_decode_partition_size(64, 40, 2048) == 512
-    assert pa.pa_decode_partition_size(256, 32, 16384) == 512
-    P = pa.pa_decode_partition_size(1, 8, 4096)
-    assert 64 <= P <= 512 and P % 16 == 0
+    assert pa.pa_decode_partition_size(64, 40, 2048) == 512    # 5120 units at 1024: < 16 waves
+    assert pa.pa_decode_partition_size(256, 32, 16384) == 1024  # 131072 units at 1024
+    assert pa.pa_decode_partition_size(16, 40, 1024) == 1024    # one partition per sequence, 640 pairs
+    assert pa.pa_decode_partition_size(8, 40, 1024) == 512      # 320 pairs: split, 640 units at 512
+    assert pa.pa_decode_partition_size(32, 40, 4096) == 512     # 5120 units at 1024
+    assert pa.pa_decode_partition_size(1, 40, 4096) == 256      # 640 units; 512 would give 320
+    assert pa.pa_decode_partition_size(1, 40, 1024) == 64       # 640 units; 128 would give 320
+    assert pa.pa_decode_partition_size(1, 8, 4096) == 64        # 512 units; 128 would give 256
+    assert pa.pa_decode_partition_size(1, 1, 4096) == 64        # floor
+    assert pa.pa_decode_partition_size(0, 40, 4096) == 512
+    for S, H, mx in ((1, 1, 1), (3, 7, 100), (1000, 64, 100000), (380, 1, 1025)):
+        P = pa.pa_decode_partition_size(S, H, mx)
+        assert P in (64, 128, 256, 512, 1024)
     for S, H, D, mx in ((64, 40, 128, 2048), (256, 32, 128, 16384), (4, 4, 64, 46)):
         n = pa.pa_decode_workspace_bytes(S, H, D, mx, 0)
         P = pa.pa_decode_partition_size(S, H, mx)

@@ -88,6 +88,46 @@ def test_prefill_fp16_tile_aligned_chunks(pa):
     assert_attn_close(out, ref, "f16", "prefill fp16")
 
 
+def test_prefill_bf16_values_outside_the_fp16_range(pa):
+    """A bf16 pool's V tiles go through the P V product in fp16, which holds
+    bf16 values exactly only below 2^16.  Place V values of 65280 (the largest
+    bf16 value below 2^16), 2^16 and beyond, in the cached context and among
+    the chunk's own tokens, in one or both halves of a key tile: rows that
+    see them must stay within the gate relative to the largest |v| they see,
+    every other row within the plain gate."""
+    m = W.small_prefill(chunk_lens=(200, 150), ctx_before=(300, 40), H=2, B=16)
+    w = m.decode
+    B = w.block_size
+    big = []  # (chunk, head, position, value)
+    for c, h, p, val in ((0, 0, 5, 3.0e5), (0, 0, 140, 65280.0), (0, 1, 200, -65536.0), (0, 1, 330, 1.0e6),
+                         (1, 0, 10, 65280.0), (1, 1, 100, -2.5e5), (1, 1, 170, 7.0e4)):
+        c0 = int(m.ctx_before[c])
+        if p < c0:  # cached context: straight into the pool
+            blk = int(m.chunk_tables[c, p // B])
+            w.v_pool[blk, h, p % B, 3] = val
+        else:       # one of the chunk's tokens, written by the scatter
+            t = int(m.chunk_lens[:c].sum()) + p - c0
+            m.chunk_v[t, h, 3] = val
+        big.append((c, h, p, abs(float(torch.tensor(val, dtype=torch.bfloat16).float()))))
+    out, flags, _, _ = run_prefill(pa, m, "f32")
+    assert flags == 0
+    ref, _, _ = oracle_prefill(m)
+    g = out.cpu().double().numpy()
+    assert np.isfinite(g).all()
+    # largest |v| each output row (token, head) attends to
+    scale = np.ones(g.shape[:2])
+    starts = [0] + np.cumsum(m.chunk_lens.numpy()).tolist()
+    for c, h, p, a in big:
+        c0 = int(m.ctx_before[c])
+        first = max(p - c0, 0)  # chunk rows at positions >= p see key p
+        rows = slice(starts[c] + first, starts[c + 1])
+        scale[rows, h] = np.maximum(scale[rows, h], a)
+    err = np.abs(g - ref).max(axis=2)
+    worst = float((err / scale).max())
+    assert worst <= 2e-3, f"relative error {worst:.3e}"
+    assert float(err[scale == 1.0].max()) <= 2e-3
+
+
 def test_prefill_rows_match_decode_at_their_positions(pa):
     """Cross-kernel: chunk row i equals pa_decode of the same query with a
     context of ctx_before + i + 1 tokens."""

@@ -32,6 +32,11 @@
  *    trap: the kernel ORs a PA_FLAG_* bit into the caller's int32 `err_flag`
  *    (device memory, zero-initialised by the caller) and skips the bad work.
  *    pa_get_error() reads and clears it.
+ *  - Threads: every kernel entry point may be called from several host
+ *    threads at once (on one device or several); the library's only
+ *    process-wide state is a per-device cache of kernel settings, filled
+ *    idempotently.  Allocator handles and decode-graph objects are not
+ *    thread-safe: one per thread, or lock around them.
  */
 #ifndef PA_H_
 #define PA_H_

@@ -5,6 +5,7 @@
 // The kernels are pure byte movers: 16-byte vector loads and stores,
 // grid-stride loops.  The scatter and the block copy are bound by HBM
 // bandwidth, the swap by the CPU-GPU link.
+#include <atomic>
 #include <cstdio>
 
 #include "pa_common.cuh"
@@ -119,11 +120,15 @@ namespace pa_host {
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  static int cached[64] = {0};
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  // per device; host threads may race to fill an entry, all with the same value
+  static std::atomic<int> cached[64];
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

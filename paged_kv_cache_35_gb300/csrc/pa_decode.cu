@@ -50,6 +50,7 @@
 //  * Every wait is bounded; bad table entries are flagged, never trapped.
 #include <math.h>
 
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -605,21 +606,23 @@ int configure_decode(int* occ_out) {
   const int smem = (int)sizeof(Smem);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  static int configured[64] = {0};
-  static int occupancy[64] = {0};
+  // resident CTAs per SM, per device; 0 until the kernel is configured there.
+  // Host threads may race to configure a device: the setup is idempotent and
+  // the value is published only after it.
+  static std::atomic<int> occupancy[64];
   if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
-  if (!configured[dev]) {
+  int occ = occupancy[dev].load(std::memory_order_acquire);
+  if (occ == 0) {
     if (cudaFuncSetAttribute(pa::decode_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return PA_ERR_CUDA;
-    int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pa::decode_kernel<D, T>, pa::kDecodeThreads, smem) !=
         cudaSuccess)
       return PA_ERR_CUDA;
-    occupancy[dev] = occ > 0 ? occ : 1;
-    configured[dev] = 1;
+    if (occ < 1) occ = 1;
+    occupancy[dev].store(occ, std::memory_order_release);
   }
-  *occ_out = occupancy[dev];
+  *occ_out = occ;
   return PA_OK;
 }
 

@@ -31,8 +31,10 @@
 //              each other; they merge by log-sum-exp once, at the end of the
 //              item.  Each thread reads its 64 scores with one tcgen05.ld,
 //              masks (only tiles on the diagonal, at the context end or with a
-//              bad page), runs the online softmax, and writes P over its own 64
-//              score columns with tcgen05.st as two 16-bit parts, P = P_hi +
+//              bad page), runs the online softmax (running max in raw score
+//              units, exponents (s - m) * scale * log2 e, so the maximum's
+//              weight is exactly 1), and writes P over its own 64 score
+//              columns with tcgen05.st as two 16-bit parts, P = P_hi +
 //              P_lo (P_hi = P in the input type, P_lo = the remainder in the
 //              input type), so that O_h += P_hi V + P_lo V carries ~16 bits
 //              of P: a single 16-bit P carries 8 (bf16) or 11 (fp16) bits, and
@@ -57,6 +59,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -98,7 +101,7 @@ struct PfBars {
   uint64_t o_free;         // every softmax warp has read the output accumulators (end of an item)
   uint64_t drain;
   uint32_t tmem_base;
-  float xm[2][kPfRows];  // half-row running max at the end: [half][row]
+  float xm[2][kPfRows];  // half-row running max (raw score) at the end: [half][row]
   float xl[2][kPfRows];  // half-row sum at the end: [half][row]
   int abort_flag;
   uint16_t order[kPfRankMax];  // (chunk, query tile) pairs, longest first
@@ -231,6 +234,45 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Two fp32 values as one 64-bit pair, and back.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// max(a, b, c) in one instruction (an operand that is NaN is ignored, as in fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a - m) * q and (b - m) * q with the packed fp32-pair instructions: one
+// subtraction and one multiplication per two values.  mm = (m, m), qq = (q, q).
+__device__ __forceinline__ float2 sub_mul_f32x2(float a, float b, uint64_t mm, uint64_t qq) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack_f32x2(a, b)), "l"(mm));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(d) : "l"(qq));
+  return unpack_f32x2(d);
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <>
@@ -252,7 +294,8 @@ template <>
 __device__ __forceinline__ void split2<__half>(float x, float y, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(x, y);
   const float2 hf = __half22float2(h);
-  const __half2 r = __floats2half2_rn(x - hf.x, y - hf.y);
+  const float2 rf = unpack_f32x2(sub_f32x2(pack_f32x2(x, y), pack_f32x2(hf.x, hf.y)));
+  const __half2 r = __floats2half2_rn(rf.x, rf.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
@@ -261,12 +304,12 @@ __device__ __forceinline__ void split2<__nv_bfloat16>(float x, float y, uint32_t
   // bf16 is the upper half of an fp32: hi keeps the upper 16 bits of x and y
   // (truncation), the remainder x - hi is exact in fp32 and is truncated the
   // same way.  hi + lo is within 2^-15 of x relative; no conversion
-  // instructions, only bit selects and two subtractions.
+  // instructions, only bit selects and one packed subtraction.
   const uint32_t xb = __float_as_uint(x), yb = __float_as_uint(y);
-  const float rx = x - __uint_as_float(xb & 0xffff0000u);
-  const float ry = y - __uint_as_float(yb & 0xffff0000u);
+  const float2 r = unpack_f32x2(sub_f32x2(pack_f32x2(x, y), pack_f32x2(__uint_as_float(xb & 0xffff0000u),
+                                                                          __uint_as_float(yb & 0xffff0000u))));
   hi = __byte_perm(xb, yb, 0x7632);
-  lo = __byte_perm(__float_as_uint(rx), __float_as_uint(ry), 0x7632);
+  lo = __byte_perm(__float_as_uint(r.x), __float_as_uint(r.y), 0x7632);
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
@@ -674,24 +717,32 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int i = 4; i < 64; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
-        const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.qscale;  // qscale > 0
+        for (int i = 4; i < 64; i += 2) mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], s[i], s[i + 1]);
+        // the running max is kept in raw score units, so that the exponent
+        // (s - m) * qscale of the row's maximum is exactly 0 and its weight
+        // exactly 1 (a rounded m * qscale would leave its rounding error there)
+        const float rmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_new = fmaxf(m_used, rmax);
-        const bool resc = m_new > m_used + kRescaleThreshold;  // also true when m_used is -inf
+        // rescale when the max grew by more than 2^kRescaleThreshold (qscale > 0);
+        // also true when m_used is -inf
+        const bool resc = (m_new - m_used) * a.qscale > kRescaleThreshold;
         const float m_next = resc ? m_new : m_used;
-        const float alpha = resc ? ((m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_next)) : 1.f;
+        const float alpha = resc ? ((m_used == -INFINITY) ? 0.f : ex2_approx((m_used - m_next) * a.qscale)) : 1.f;
         l *= alpha;
         const float mref = (m_next == -INFINITY) ? 0.f : m_next;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t mm2 = pack_f32x2(mref, mref), qq2 = pack_f32x2(a.qscale, a.qscale);
+        uint64_t sum2[2] = {0, 0};  // packed (even, odd) partial sums; 0 bits = (0.f, 0.f)
         uint32_t hw[32], lw[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2_approx(fmaf(s[2 * e], a.qscale, -mref));
-          const float p1 = ex2_approx(fmaf(s[2 * e + 1], a.qscale, -mref));
-          sum4[e & 3] += p0 + p1;
+          const float2 x2 = sub_mul_f32x2(s[2 * e], s[2 * e + 1], mm2, qq2);
+          const float p0 = ex2_approx(x2.x);
+          const float p1 = ex2_approx(x2.y);
+          sum2[e & 1] = add_f32x2(sum2[e & 1], pack_f32x2(p0, p1));
           split2<T>(p0, p1, hw[e], lw[e]);
         }
-        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        const float2 sa = unpack_f32x2(sum2[0]), sb2 = unpack_f32x2(sum2[1]);
+        l += (sa.x + sa.y) + (sb2.x + sb2.y);
         // This half's columns of the buffer held P_h(x-2): wait for P_h(x-2) V.
         // A rescale of O_h also needs P_h(x-1) V (same item) in it.
         const bool any_resc = t > 0 && __any_sync(0xffffffffu, resc);
@@ -765,8 +816,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc_fence_after();
       const float m0 = bars.xm[0][r], m1 = bars.xm[1][r];
       const float M = fmaxf(m0, m1);
-      const float w0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - M);
-      const float w1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
+      const float w0 = m0 == -INFINITY ? 0.f : ex2_approx((m0 - M) * a.qscale);
+      const float w1 = m1 == -INFINITY ? 0.f : ex2_approx((m1 - M) * a.qscale);
       const float lt = w0 * bars.xl[0][r] + w1 * bars.xl[1][r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float c0w = w0 * inv, c1w = w1 * inv;
@@ -977,12 +1028,13 @@ int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_
   const int variant = (dtype == PA_BF16 ? 1 : 0) + (head_dim == 128 ? 2 : 0);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
-  static int configured[4][64] = {{0}};
-  if (!configured[variant][dev]) {
+  // per kernel variant and device; host threads may race to configure (idempotent)
+  static std::atomic<bool> configured[4][64];
+  if (!configured[variant][dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pa::kPfSmemBytes) !=
         cudaSuccess)
       return PA_ERR_CUDA;
-    configured[variant][dev] = 1;
+    configured[variant][dev].store(true, std::memory_order_release);
   }
   const long long n_items = (long long)a.qtiles * num_chunks * num_heads;
   const int sms = device_sm_count();

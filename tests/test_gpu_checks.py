@@ -121,3 +121,65 @@ def test_a_wait_that_runs_out_flags_timeout_and_the_context_stays_usable(pa):
                  w.context_lens.to(dev), 300, w.scale, ws, err)
     assert pa.pa_get_error(err) == 0
     assert torch.isfinite(out).all()
+
+
+THREADS_SCRIPT = r"""
+import threading
+import torch
+import paged_kv_cache_35_gb300 as pa
+import pa_workloads as W
+
+dev = torch.device("cuda")
+torch.cuda.set_device(0)
+w = W.small_decode(ctx=(1, 17, 300, 1029), H=2, dtype="bf16")
+m = W.small_prefill(chunk_lens=(130, 77), ctx_before=(200, 37), H=3)
+S, H, D, mx = w.num_seqs, w.num_heads, w.head_dim, int(w.context_lens.max())
+kp, vp, tb, cl, q = (t.to(dev) for t in (w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.q))
+mk, mv, mt = m.decode.k_pool.to(dev), m.decode.v_pool.to(dev), m.chunk_tables.to(dev)
+cu = torch.cat([torch.zeros(1, dtype=torch.int32), m.chunk_lens.cumsum(0).to(torch.int32)]).to(dev)
+cb, mq = m.ctx_before.to(dev), m.chunk_q.to(dev)
+T = int(m.chunk_lens.sum())
+n = 4
+streams = [torch.cuda.Stream() for _ in range(n)]
+outs = [torch.empty(S, H, D, dtype=torch.float32, device=dev) for _ in range(n)]
+pouts = [torch.empty(T, 3, D, dtype=torch.float32, device=dev) for _ in range(n)]
+wss = [pa.decode_workspace(S, H, D, mx) for _ in range(n)]
+errs = [pa.new_error_flag() for _ in range(n)]
+torch.cuda.synchronize()
+start = threading.Barrier(n)
+status = [None] * n
+
+def work(i):
+    try:
+        start.wait()
+        # the first decode and prefill calls of this process, from n threads at once
+        pa.pa_decode(outs[i], q, kp, vp, tb, cl, mx, w.scale, wss[i], errs[i], stream=streams[i])
+        pa.pa_prefill_chunk(pouts[i], mq, cu, cb, mk, mv, mt, int(m.chunk_lens.max()), m.decode.scale, errs[i],
+                            stream=streams[i])
+        status[i] = "ok"
+    except Exception as e:  # reported below
+        status[i] = repr(e)
+
+ths = [threading.Thread(target=work, args=(i,)) for i in range(n)]
+for t in ths:
+    t.start()
+for t in ths:
+    t.join()
+torch.cuda.synchronize()
+assert status == ["ok"] * n, status
+assert all(pa.pa_get_error(e) == 0 for e in errs)
+for i in range(1, n):
+    assert torch.equal(outs[i], outs[0]) and torch.equal(pouts[i], pouts[0]), i
+assert torch.isfinite(outs[0]).all() and torch.isfinite(pouts[0]).all()
+print("threads ok")
+"""
+
+
+def test_first_calls_from_several_host_threads_at_once(pa):
+    """The per-device kernel settings are filled on first use; four host
+    threads making their first decode and prefill calls at the same time, on
+    their own streams, must all launch and agree bit for bit (run in a fresh
+    process so that these really are the first calls)."""
+    r = subprocess.run([sys.executable, "-c", THREADS_SCRIPT], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().splitlines()[-1] == "threads ok"

@@ -128,6 +128,49 @@ def test_prefill_bf16_values_outside_the_fp16_range(pa):
     assert float(err[scale == 1.0].max()) <= 2e-3
 
 
+@pytest.mark.parametrize("hot", [0, 150, 207, 263, 499])
+def test_prefill_one_hot_key_is_bitwise(pa, hot):
+    """Every query of the chunk equals q0 and the key at position `hot` is
+    32 q0 (per head), so for each row that sees it every other weight
+    underflows to 0: the output row is V[hot] bit for bit.  Sweeping `hot`
+    over the cached context and the chunk's own tokens (several key tiles and
+    16-token pages) checks the paged indexing of the prefill kernel exactly.
+    Rows before `hot` are checked against the oracle within the gate."""
+    m = W.small_prefill(chunk_lens=(300,), ctx_before=(200,), H=2, B=16)
+    w = m.decode
+    B, c0 = w.block_size, int(m.ctx_before[0])
+    g = torch.Generator().manual_seed(11)
+    q0 = torch.randn(w.num_heads, w.head_dim, generator=g).to(m.chunk_q.dtype)
+    m.chunk_q[:] = q0
+    key = (32.0 * q0.float()).to(m.chunk_q.dtype)
+    if hot < c0:
+        blk = int(m.chunk_tables[0, hot // B])
+        w.k_pool[blk, :, hot % B, :] = key
+        v_hot = w.v_pool[blk, :, hot % B, :].float()
+    else:
+        m.chunk_k[hot - c0] = key
+        v_hot = m.chunk_v[hot - c0].float()
+    out, flags, _, _ = run_prefill(pa, m, "f32")
+    assert flags == 0
+    got = out.cpu()
+    first = max(hot - c0, 0)  # chunk rows at positions >= hot see the key
+    assert torch.equal(got[first:], v_hot.expand(300 - first, -1, -1)), "one-hot rows differ from V[hot]"
+    if first > 0:
+        ref, _, _ = oracle_prefill(m)
+        assert_attn_close(got[:first], ref[:first], "f32", f"rows before key {hot}")
+
+
+def test_prefill_single_key_row_is_v0_bitwise(pa):
+    """A chunk at context 0: its first row attends to one key, its own
+    token, so its output is that token's V row exactly (exp(0) = 1)."""
+    m = W.small_prefill(chunk_lens=(5, 130), ctx_before=(0, 0), H=3, B=16)
+    out, flags, _, _ = run_prefill(pa, m, "f32")
+    assert flags == 0
+    got = out.cpu()
+    assert torch.equal(got[0], m.chunk_v[0].float())
+    assert torch.equal(got[5], m.chunk_v[5].float())
+
+
 def test_prefill_rows_match_decode_at_their_positions(pa):
     """Cross-kernel: chunk row i equals pa_decode of the same query with a
     context of ctx_before + i + 1 tokens."""

@@ -34,14 +34,16 @@
 //              bad page), runs the online softmax (running max in raw score
 //              units, exponents (s - m) * scale * log2 e, so the maximum's
 //              weight is exactly 1), and writes P over its own 64 score
-//              columns with tcgen05.st as two 16-bit parts, P = P_hi +
-//              P_lo (P_hi = P in the input type, P_lo = the remainder in the
-//              input type), so that O_h += P_hi V + P_lo V carries ~16 bits
-//              of P: a single 16-bit P carries 8 (bf16) or 11 (fp16) bits, and
-//              its rounding alone moves a peaked row's output by ~2^-9 |v|.
+//              columns with tcgen05.st.  In a bf16 pool P is two bf16 parts,
+//              P = P_hi + P_lo (upper 16 bits of P and of the remainder), so
+//              that O_h += P_hi V + P_lo V carries ~16 bits of P: a single
+//              bf16 P carries 8 bits, and its rounding alone moves a peaked
+//              row's output by ~2^-9 |v|.  In an fp16 pool P is one fp16
+//              value (11 bits, kept at 2^7 x the numerator) and one product
+//              O_h += P V, the row sum adding the rounded values.
 //    The MMA thread issues S(0), S(1), then per key tile j: P_0(j) V, P_1(j)
-//    V, S(j+2): the score buffer of tile j+1 is ready while the softmax of
-//    tile j runs.  An output accumulator is rescaled lazily (only when its
+//    V (two parts each in a bf16 pool), S(j+2): the score buffer of tile j+1
+//    is ready while the softmax of tile j runs.  An output accumulator is rescaled lazily (only when its
 //    half-row max grew by more than 2^8: it is read, scaled and written back
 //    in tensor memory); only then does the softmax of tile j wait for
 //    P_h(j-1) V, otherwise it overlaps it.  Ring stages and barrier phases
@@ -62,6 +64,7 @@
 #include <atomic>
 #include <cstdio>
 #include <mutex>
+#include <type_traits>
 
 #include "pa_common.cuh"
 
@@ -77,6 +80,11 @@ constexpr int kVStages = 3;
 constexpr uint32_t kHalfBytes = kPfRows * 64 * 2;  // 128 rows x 64 columns x 2 bytes
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;     // one 128 x 128 16-bit tile
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
+// An fp16 pool's P is one fp16 value kept at 2^7 times the softmax
+// numerator: with the lazy rescale its largest value is 2^(8+7), inside the
+// fp16 range, and weights down to 2^-21 of the row maximum keep full fp16
+// precision (the scale cancels in the final division by the row sum).
+constexpr float kPScaleLog2 = 7.0f;
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: two score buffers (later P) and the two half-row outputs
 __device__ __forceinline__ uint32_t tmem_s(int b) { return b ? 128u : 0u; }
@@ -286,25 +294,12 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// (x, y) as two packed 16-bit pairs: hi = (x, y) rounded to T, lo = the
-// remainders rounded to T, so that hi + lo carries ~16 significant bits.
-template <typename T>
-__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo);
-template <>
-__device__ __forceinline__ void split2<__half>(float x, float y, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(x, y);
-  const float2 hf = __half22float2(h);
-  const float2 rf = unpack_f32x2(sub_f32x2(pack_f32x2(x, y), pack_f32x2(hf.x, hf.y)));
-  const __half2 r = __floats2half2_rn(rf.x, rf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&r);
-}
-template <>
-__device__ __forceinline__ void split2<__nv_bfloat16>(float x, float y, uint32_t& hi, uint32_t& lo) {
-  // bf16 is the upper half of an fp32: hi keeps the upper 16 bits of x and y
-  // (truncation), the remainder x - hi is exact in fp32 and is truncated the
-  // same way.  hi + lo is within 2^-15 of x relative; no conversion
-  // instructions, only bit selects and one packed subtraction.
+// (x, y) as two packed bf16 pairs, hi + lo carrying ~16 significant bits.
+// bf16 is the upper half of an fp32: hi keeps the upper 16 bits of x and y
+// (truncation), the remainder x - hi is exact in fp32 and is truncated the
+// same way.  hi + lo is within 2^-15 of x relative; no conversion
+// instructions, only bit selects and one packed subtraction.
+__device__ __forceinline__ void split2_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
   const uint32_t xb = __float_as_uint(x), yb = __float_as_uint(y);
   const float2 r = unpack_f32x2(sub_f32x2(pack_f32x2(x, y), pack_f32x2(__uint_as_float(xb & 0xffff0000u),
                                                                           __uint_as_float(yb & 0xffff0000u))));
@@ -415,6 +410,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   constexpr int kHalves = D / 64;
   constexpr uint32_t kLoadBytes = kHalves * kHalfBytes;  // bytes of one loaded Q, K or V tile
+  // P V as P_hi V + P_lo V in bf16 (bf16 pool: 8-bit P alone is not accurate
+  // enough), or as one product with an fp16 P (fp16 pool: 11 bits are)
+  constexpr int kPParts = std::is_same<T, __nv_bfloat16>::value ? 2 : 1;
   // a kernel launched behind this one as a programmatic dependent may start
   // as soon as every CTA is resident (pa_mixed_step's decode); it must not
   // read this kernel's output without waiting for it
@@ -633,7 +631,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {  // P_hi V, then P_lo V
+            for (int part = 0; part < kPParts; ++part) {  // P V, or P_hi V then P_lo V
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 umma_f16_ts(tmem + tmem_o(hh), pb + hh * 64 + part * 32 + kk * 8,
@@ -736,10 +734,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float2 x2 = sub_mul_f32x2(s[2 * e], s[2 * e + 1], mm2, qq2);
-          const float p0 = ex2_approx(x2.x);
-          const float p1 = ex2_approx(x2.y);
-          sum2[e & 1] = add_f32x2(sum2[e & 1], pack_f32x2(p0, p1));
-          split2<T>(p0, p1, hw[e], lw[e]);
+          if (kPParts == 2) {
+            const float p0 = ex2_approx(x2.x);
+            const float p1 = ex2_approx(x2.y);
+            sum2[e & 1] = add_f32x2(sum2[e & 1], pack_f32x2(p0, p1));
+            split2_bf16(p0, p1, hw[e], lw[e]);
+          } else {
+            // fp16 P at 2^7 x the numerator; the row sum adds the rounded
+            // values the product uses, so a weight's rounding moves the
+            // output by at most 2^-11 w |v - o|
+            const __half2 h2 = __floats2half2_rn(ex2_approx(x2.x + kPScaleLog2), ex2_approx(x2.y + kPScaleLog2));
+            sum2[e & 1] = add_f32x2(sum2[e & 1], pack_f32x2(__low2float(h2), __high2float(h2)));
+            hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
         }
         const float2 sa = unpack_f32x2(sum2[0]), sb2 = unpack_f32x2(sum2[1]);
         l += (sa.x + sa.y) + (sb2.x + sb2.y);
@@ -754,12 +761,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         tc_fence_after();
-        // P_h over this half's scores: P_hi in its first 32 words, P_lo in the next 32
+        // P_h over this half's scores: P (or P_hi) in its first 32 words, P_lo in the next 32
         const uint32_t pw = s_half + tmem_s(sb);
         tmem_st16(pw, hw);
         tmem_st16(pw + 16, hw + 16);
-        tmem_st16(pw + 32, lw);
-        tmem_st16(pw + 48, lw + 16);
+        if (kPParts == 2) {
+          tmem_st16(pw + 32, lw);
+          tmem_st16(pw + 48, lw + 16);
+        }
         if (any_resc) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {

@@ -128,15 +128,16 @@ def test_prefill_bf16_values_outside_the_fp16_range(pa):
     assert float(err[scale == 1.0].max()) <= 2e-3
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("hot", [0, 150, 207, 263, 499])
-def test_prefill_one_hot_key_is_bitwise(pa, hot):
+def test_prefill_one_hot_key_is_bitwise(pa, hot, dtype):
     """Every query of the chunk equals q0 and the key at position `hot` is
     32 q0 (per head), so for each row that sees it every other weight
     underflows to 0: the output row is V[hot] bit for bit.  Sweeping `hot`
     over the cached context and the chunk's own tokens (several key tiles and
     16-token pages) checks the paged indexing of the prefill kernel exactly.
     Rows before `hot` are checked against the oracle within the gate."""
-    m = W.small_prefill(chunk_lens=(300,), ctx_before=(200,), H=2, B=16)
+    m = W.small_prefill(chunk_lens=(300,), ctx_before=(200,), H=2, B=16, dtype=dtype)
     w = m.decode
     B, c0 = w.block_size, int(m.ctx_before[0])
     g = torch.Generator().manual_seed(11)
@@ -160,10 +161,11 @@ def test_prefill_one_hot_key_is_bitwise(pa, hot):
         assert_attn_close(got[:first], ref[:first], "f32", f"rows before key {hot}")
 
 
-def test_prefill_single_key_row_is_v0_bitwise(pa):
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_single_key_row_is_v0_bitwise(pa, dtype):
     """A chunk at context 0: its first row attends to one key, its own
     token, so its output is that token's V row exactly (exp(0) = 1)."""
-    m = W.small_prefill(chunk_lens=(5, 130), ctx_before=(0, 0), H=3, B=16)
+    m = W.small_prefill(chunk_lens=(5, 130), ctx_before=(0, 0), H=3, B=16, dtype=dtype)
     out, flags, _, _ = run_prefill(pa, m, "f32")
     assert flags == 0
     got = out.cpu()

@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per pa_decode call on this workload, from the ncu
 # capture summarised in profiles/; valid only for the decode kernel source
 # whose sha256 prefix is given (otherwise reported as null).
-TRAFFIC = {"bytes_per_launch": 1488333120, "kernel_sha256_prefix": "7ca75438be1ad397",
+TRAFFIC = {"bytes_per_launch": 1488338856, "kernel_sha256_prefix": "a53b700b600e6a63",
            "source": "profiles/decode_kernel_llama13b_b64.md"}
 
 

@@ -180,7 +180,9 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
  * workspace: device memory of at least pa_decode_workspace_bytes(...) bytes,
  *   16-byte aligned; no initial contents required; not to be shared by two
  *   pa_decode calls that may run at the same time.
- * partition_size: 0 = automatic, else a multiple of 16 in [16, 1024].
+ * partition_size: 0 = automatic, else a multiple of 16 in [16, 1024];
+ *   ceil(max_context_len / partition) must stay below 2^20 (up to 2^24
+ *   tokens at partition 16, 2^30 at 1024), else PA_ERR_UNSUPPORTED.
  * A table entry outside [0, num_blocks) sets PA_FLAG_BAD_BLOCK; the 16-token
  * chunk it covers is left out of that sequence's sum.
  * Launches: a one-CTA planning kernel, then the persistent decode kernel, on

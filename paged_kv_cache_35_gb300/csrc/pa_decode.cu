@@ -592,8 +592,12 @@ WsLayout ws_layout(int S, int H, int D, int max_parts) {
   return w;
 }
 
-// Partitions of the longest sequence.
-int decode_max_parts(int max_ctx, int P) { return max_ctx > 0 ? (max_ctx + P - 1) / P : 1; }
+// Partitions of the longest sequence (no overflow near INT_MAX).
+int decode_max_parts(int max_ctx, int P) { return max_ctx > 0 ? (max_ctx - 1) / P + 1 : 1; }
+
+// A work item packs a sequence's partition count above 11 bits of token count
+// into one int32: fewer than 2^20 partitions per sequence.
+constexpr int kMaxPartsPerSeq = 1 << 20;
 
 int resolve_partition(int S, int H, int max_ctx, int partition_size) {
   if (partition_size == 0) return pa_decode_partition_size(S, H, max_ctx);
@@ -722,6 +726,7 @@ int decode_setup(void* out, int out_dtype, const void* q, const void* k_pool, co
   const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
   if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return PA_ERR_INVALID_ARG;
   const int max_parts = decode_max_parts(max_context_len, P);
+  if (max_parts >= kMaxPartsPerSeq) return PA_ERR_UNSUPPORTED;
   const WsLayout w = ws_layout(num_seqs, num_heads, head_dim, max_parts);
   if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
 
@@ -795,6 +800,7 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
   const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
   if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return 0;
   const int max_parts = decode_max_parts(max_context_len, P);
+  if (max_parts >= kMaxPartsPerSeq) return 0;
   return ws_layout(num_seqs, num_heads, head_dim, max_parts).total;
 }
 

@@ -364,8 +364,11 @@ __device__ __forceinline__ int pf_item(const PrefillArgs& a, const uint16_t* ord
   it.row0 = qt * kPfRows;
   if (it.row0 >= it.n_c) return kItemEmpty;
   it.c0 = __ldg(a.ctx_before + c);
-  it.ctx_total = it.c0 + it.n_c;
-  if (it.c0 < 0 || (int64_t)it.ctx_total > (int64_t)a.max_blocks_per_seq * a.block_size) return kItemBadLength;
+  // the context must fit the table and keep key positions well inside int32
+  const int64_t total = (int64_t)it.c0 + it.n_c;
+  if (it.c0 < 0 || total > (int64_t)a.max_blocks_per_seq * a.block_size || total > INT32_MAX - 2 * kPfKeys)
+    return kItemBadLength;
+  it.ctx_total = (int)total;
   it.rows = min(kPfRows, it.n_c - it.row0);
   it.n_kv = (it.c0 + it.row0 + it.rows - 1) / kPfKeys + 1;
   it.need_zero = it.n_kv * kPfKeys > it.ctx_total;

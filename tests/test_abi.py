@@ -68,6 +68,10 @@ def test_bad_arguments_are_rejected_before_launch(pa):
     args[15] = pa.PA_F16
     args[17] = 16  # workspace too small
     assert L.pa_decode(*args) == pa.PA_ERR_WORKSPACE
+    # 2^20 partitions of the longest sequence (max_context_len 2^24, partition 16): unsupported
+    big = list(args)
+    big[8], big[17], big[18] = 1 << 24, 1 << 40, 16
+    assert L.pa_decode(*big) == pa.PA_ERR_UNSUPPORTED
     args[17] = 1 << 20
     args[18] = 24  # partition not a multiple of 16
     assert L.pa_decode(*args) == pa.PA_ERR_INVALID_ARG
@@ -113,6 +117,11 @@ def test_partition_and_workspace_sizes(pa):
         assert n >= 4 * S * H * parts * (D + 2) and n % 256 == 0
     assert pa.pa_decode_workspace_bytes(4, 4, 64, 100, 24) == 0
     assert pa.pa_decode_workspace_bytes(4, 4, 64, 100, 2048) == 0
+    # a work item holds fewer than 2^20 partitions of one sequence
+    assert pa.pa_decode_workspace_bytes(1, 1, 128, (1 << 24) - 16, 16) > 0   # 2^20 - 1 partitions
+    assert pa.pa_decode_workspace_bytes(1, 1, 128, 1 << 24, 16) == 0          # 2^20 partitions
+    assert pa.pa_decode_workspace_bytes(1, 1, 128, (1 << 30) - 1024, 1024) > 0  # 2^20 - 1 partitions
+    assert pa.pa_decode_workspace_bytes(1, 1, 128, 2 ** 31 - 1, 1024) == 0      # 2^21: refused, no overflow
 
 
 def test_slot_mapping_matches_the_oracle(pa):

@@ -201,6 +201,13 @@ WORKLOAD_TEXT["memsim"] = ("host-only memory simulator: seeded long-tailed and s
                            "32768 tokens, reservation baselines (first fit) vs paged blocks of 16")
 WORKLOAD_TEXT["batch_sweep"] = ("decode latency vs batch size 1..256, contexts of 1024, 40 heads x 128, fp16: "
                                 "16-token pages at random places vs one contiguous 1024-token block per sequence")
+WORKLOAD_TEXT["prefill"] = ("prefill of 4 prompts x 2048 tokens at context 0, 40 heads x 128, page 256, bf16: "
+                            "the prompts' K/V scattered into the pool, then causal paged attention on the tensor "
+                            "cores (one pa_prefill_chunk call)")
+WORKLOAD_TEXT["prefill_f16"] = ("prefill of 4 prompts x 2048 tokens at context 0, 40 heads x 128, page 256, fp16: "
+                                "the prompts' K/V scattered into the pool, then causal paged attention on the "
+                                "tensor cores (one pa_prefill_chunk call)")
+PREFILL_METRIC = "chunked prefill: causal paged attention TFLOP/s (4 * head_dim * heads per admissible key)"
 WORKLOAD_TEXT["prefix_cache"] = ("prefix caching: 16 requests = a shared 1024-token system prompt + 256 tokens of "
                                  "their own, 40 heads x 128, block 16, bf16; suffix prefill over cached blocks vs "
                                  "whole-prompt prefill")
@@ -639,6 +646,198 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, rank, world, local):
+    """One prefill step = four 2048-token prompts' K/V scattered into their
+    pages, then one pa_prefill_chunk over the four prompts (context 0).  value: algorithmic
+    TFLOP/s of the step; roofline: the prefill kernel alone (per-call events
+    on every 16th step), against the measured dense tensor peak (fp16 and
+    bf16 run at the same rate); e2e: pinned host inputs in and the output
+    out every step, copies pipelined; cpu_baseline: the oracle on four
+    16-row sub-chunks spread over the first prompt (a sub-chunk starting at
+    row a has context a, so its rows are exactly those rows of the prompt)."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_35_gb300 as pa
+    import pa_workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload
+    dtype = "f16" if name == "prefill_f16" else "bf16"
+    NP, L = 4, 2048  # prompts, tokens per prompt
+    T = NP * L
+    m = W.small_prefill(device=dev, chunk_lens=(L,) * NP, ctx_before=(0,) * NP, H=40, B=256, dtype=dtype)
+    w = m.decode
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    tdt = torch.float16 if dtype == "f16" else torch.bfloat16
+    slots = pa.pa_slot_mapping(m.chunk_tables, np.repeat(np.arange(NP), L), np.tile(np.arange(L), NP), B)
+    slots_d = torch.from_numpy(slots).to(dev)
+    cu_d = torch.arange(0, T + 1, L, dtype=torch.int32, device=dev)
+    cb_d = torch.zeros(NP, dtype=torch.int32, device=dev)
+    tab_d = m.chunk_tables.to(dev)
+    out = torch.empty(T, H, D, dtype=tdt, device=dev)
+    err = pa.new_error_flag(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill(o=None, q=None, cu=None, cb=None, tab=None):
+        pick = lambda given, resident: resident if given is None else given
+        pa.pa_prefill_chunk(pick(o, out), pick(q, m.chunk_q), pick(cu, cu_d), pick(cb, cb_d), w.k_pool, w.v_pool,
+                            pick(tab, tab_d), L, w.scale, err, stream)
+
+    def step():
+        pa.pa_reshape_and_cache(m.chunk_k, m.chunk_v, w.k_pool, w.v_pool, slots_d, err, stream)
+        prefill()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    flags = pa.pa_get_error(err, stream)
+    if flags:
+        raise RuntimeError(f"device error flags {flags} during warm-up")
+    flops = NP * 4 * D * H * L * (L + 1) // 2
+
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    sampled = list(range(0, K, 16))
+    p_s, p_e = {i: ev() for i in sampled}, {i: ev() for i in sampled}
+    t_start, t_end = ev(), ev()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    h0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        pa.pa_reshape_and_cache(m.chunk_k, m.chunk_v, w.k_pool, w.v_pool, slots_d, err, stream)
+        if i in p_s:
+            p_s[i].record(stream)
+            prefill()
+            p_e[i].record(stream)
+        else:
+            prefill()
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    h1 = time.time()
+    dist_barrier(world)
+    clocks.stop()
+    flags = pa.pa_get_error(err, stream)
+    if flags:
+        raise RuntimeError(f"device error flags {flags} in the timed region")
+    max_ms = dist_max(t_start.elapsed_time(t_end), world)
+    value = flops * K * world / (max_ms / 1e3) / 1e12
+    pre_ms = [p_s[i].elapsed_time(p_e[i]) for i in sampled]
+
+    # ---- end to end: pinned host inputs (q, the prompt's K/V, slots, table,
+    # offsets) in and the output out every step, double-buffered on their own streams
+    Ke = min(K, 200)
+    pin = lambda t: t.detach().cpu().pin_memory()
+    host_in = [pin(m.chunk_q), pin(m.chunk_k), pin(m.chunk_v), pin(torch.from_numpy(slots)), pin(m.chunk_tables),
+               pin(cu_d), pin(cb_d)]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    bufs_in = [[torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_in] for _ in range(2)]
+    bufs_out = [torch.empty_like(out) for _ in range(2)]
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+    for b in range(2):
+        done[b].record(stream)
+        drained[b].record(stream)
+
+    def e2e_step(i):
+        b = i % 2
+        d_in, d_out = bufs_in[b], bufs_out[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(done[b])
+            for d, h in zip(d_in, host_in):
+                d.copy_(h, non_blocking=True)
+            ready[b].record(s_in)
+        stream.wait_event(ready[b])
+        stream.wait_event(drained[b])
+        d_q, d_k, d_v, d_slots, d_tab, d_cu, d_cb = d_in
+        pa.pa_reshape_and_cache(d_k, d_v, w.k_pool, w.v_pool, d_slots, err, stream)
+        prefill(d_out, d_q, d_cu, d_cb, d_tab)
+        done[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[b])
+            host_out.copy_(d_out, non_blocking=True)
+            drained[b].record(s_out)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    dist_barrier(world)
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    s_in.wait_event(e0)
+    for i in range(Ke):
+        e2e_step(i)
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist_max(e0.elapsed_time(e1), world)
+    if not torch.equal(host_out.view(torch.int16), out.cpu().view(torch.int16)):
+        raise RuntimeError("the end-to-end result differs from the device-timed step's")
+    if pa.pa_get_error(err, stream):
+        raise RuntimeError("device error flags in the end-to-end pass")
+
+    peak, peak_kind = load_tensor_peak()
+    pre_avg_s = statistics.mean(pre_ms) / 1e3
+    achieved = flops / pre_avg_s / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[name], "prompts": NP, "tokens_per_prompt": L, "context_before": 0,
+                   "num_heads": H, "head_dim": D, "block_size": B, "kv_dtype": dtype,
+                   "l2": "no flush: inputs larger than L2 (per step the scatter reads 168 MB of new K/V and "
+                         "writes it to the pool, the prefill reads it and 84 MB of queries and writes 84 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "prefill_kernel (pa_prefill_chunk)", "algorithmic_flops_per_launch": flops,
+                     "avg_launch_ms": pre_avg_s * 1e3, "timed_calls": len(pre_ms),
+                     "tensor_flops_executed_per_launch": flops * (3 if dtype == "bf16" else 2) // 2,
+                     "note": "bf16: P V runs as two products (P_hi, P_lo); fp16: one"},
+        "e2e": {"value": flops * Ke * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / Ke, "steps": Ke,
+                "overlap": "copies on their own streams, double-buffered, overlapping the previous step"},
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(h0, h1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+
+        kb, vb = oracle.pool_bits(w.k_pool.cpu()), oracle.pool_bits(w.v_pool.cpu())
+        oracle.reshape_and_cache(m.chunk_k.cpu(), m.chunk_v.cpu(), kb, vb, slots, B)
+        starts, n = (0, 672, 1344, 2032), 16
+        q_host = m.chunk_q.cpu()
+        q_s = torch.cat([q_host[a:a + n] for a in starts])
+        cu_s = torch.arange(0, n * len(starts) + 1, n, dtype=torch.int32)
+        cb_s = torch.tensor(starts, dtype=torch.int32)
+        tab_s = m.chunk_tables.cpu()[:1].expand(len(starts), -1).contiguous()
+        s_flops = sum(4 * D * H * (a + i + 1) for a in starts for i in range(n))
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.prefill(q_s, cu_s, cb_s, kb, vb, tab_s, B, w.scale, dtype)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= args.cpu_budget or reps >= 1000:
+                break
+        line["cpu_baseline"] = {"value": s_flops * reps / el / 1e12, "unit": "TFLOP/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{len(starts)} x {n} query rows (contexts 1..{starts[-1] + n}), "
+                                          f"{reps} repetitions, {el:.1f} s wall"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def graph_replay_comparison(pa, w, dev, stream, n=2000):
     """The decode step issued as a direct pa_decode call and as a replay of
     its recorded CUDA graph (DecodeGraphs, sequence interval 8, KV interval
@@ -985,6 +1184,8 @@ def main():
         run_prefix_cache(args, rank, world, local)
     elif args.workload == "batch_sweep":
         run_batch_sweep(args, rank, world, local)
+    elif args.workload in ("prefill", "prefill_f16"):
+        run_prefill(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

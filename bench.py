@@ -804,7 +804,8 @@ def run_prefill(args, rank, world, local):
                      "kernel": "prefill_kernel (pa_prefill_chunk)", "algorithmic_flops_per_launch": flops,
                      "avg_launch_ms": pre_avg_s * 1e3, "timed_calls": len(pre_ms),
                      "tensor_flops_executed_per_launch": flops * (3 if dtype == "bf16" else 2) // 2,
-                     "note": "bf16: P V runs as two products (P_hi, P_lo); fp16: one"},
+                     "note": "bf16: P V runs as two products (P_hi, P_lo); fp16: one. DRAM traffic of one "
+                             "bf16 launch: profiles/prefill_kernel_4x2048.md"},
         "e2e": {"value": flops * Ke * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / Ke, "steps": Ke,
                 "overlap": "copies on their own streams, double-buffered, overlapping the previous step"},

@@ -94,7 +94,11 @@ __device__ __forceinline__ uint32_t tmem_o(int h) { return h ? 384u : 256u; }
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;             // kKStages stages
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;  // kVStages stages
-constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
+// Output staging: 2 KB per softmax warp, 32 rows x 64 bytes, so that a warp
+// stores whole 64-byte row pieces instead of one 16-byte piece per row.
+constexpr uint32_t kStageBytes = 32 * 64;
+constexpr uint32_t kOffStage = kOffV + kVStages * kTileBytes;
+constexpr uint32_t kOffBar = kOffStage + 8 * kStageBytes;
 constexpr int kPfRankMax = 1024;  // (chunk, query tile) pairs ranked in-kernel
 
 struct PfBars {
@@ -666,14 +670,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int p = t * kPfKeys + lane * rpl;
         return (t < n_kv && lane < pieces && p < ctx_total) ? __ldg(trow + p / B) : -1;
       };
-      int32_t entry_next = piece_entry(0);
+      // Every table entry the item reads in range: then no key tile needs a
+      // per-piece mask and the per-tile lookups are skipped.
+      bool all_ok;
+      {
+        const int kend = min(ctx_total, n_kv * kPfKeys);
+        const int npages = (kend + B - 1) / B;
+        bool bad = false;
+#pragma unroll 4
+        for (int p = lane; p < npages; p += 32) {
+          const int32_t e = __ldg(trow + p);
+          bad |= (e < 0 || e >= a.num_blocks);
+        }
+        all_ok = !__any_sync(0xffffffffu, bad);
+      }
+      int32_t entry_next = all_ok ? 0 : piece_entry(0);
       float m_used = -INFINITY;
       float l = 0.f;
       for (int t = 0; t < n_kv; ++t) {
         const int x = g + t;
         const int sb = x & 1;
-        const uint32_t kmask = __ballot_sync(0xffffffffu, entry_next >= 0 && entry_next < a.num_blocks);
-        entry_next = piece_entry(t + 1);
+        uint32_t kmask = full_mask;
+        if (!all_ok) {
+          kmask = __ballot_sync(0xffffffffu, entry_next >= 0 && entry_next < a.num_blocks);
+          entry_next = piece_entry(t + 1);
+        }
         ok = mbar_wait(&bars.s_full[sb], (x >> 1) & 1, abort_flag, a.err_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -732,11 +753,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         const float2 sa = unpack_f32x2(sum2[0]), sb2 = unpack_f32x2(sum2[1]);
         l += (sa.x + sa.y) + (sb2.x + sb2.y);
-        // This half's columns of the buffer held P_h(x-2): wait for P_h(x-2) V.
+        // This half's columns of the buffer held P_h(x-2).  Its P V needs no
+        // wait: S(x) was issued after it, and a commit tracks every earlier
+        // MMA of the issuing thread, so S(x) complete means P_h(x-2) V is too.
         // A rescale of O_h also needs P_h(x-1) V (same item) in it.
         const bool any_resc = t > 0 && __any_sync(0xffffffffu, resc);
-        if (x >= 2) ok = mbar_wait(&bars.pv_done[half][sb], ((x - 2) >> 1) & 1, abort_flag, a.err_flag);
-        if (ok && any_resc)
+        if (any_resc)
           ok = mbar_wait(&bars.pv_done[half][(x - 1) & 1], ((x - 1) >> 1) & 1, abort_flag, a.err_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -812,9 +834,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float lt = w0 * bars.xl[0][r] + w1 * bars.xl[1][r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float c0w = w0 * inv, c1w = w1 * inv;
-      const bool store = qrow < it.n_c;
-      const int ocol0 = half * (D / 2);  // this thread writes output columns ocol0 .. ocol0 + D/2 - 1
-      const size_t obase = ((size_t)(it.q0 + qrow) * H + it.h) * D + ocol0;
+      // This warp's 32 rows x 64 output columns leave through its staging slab
+      // in 64-byte row pieces: a thread writes its row's piece (16-byte unit j
+      // at j ^ ((row >> 1) & 3), so that 8 consecutive rows cover all banks),
+      // then four lanes per row store 8 rows at a time.
+      const int ocol0 = half * (D / 2);  // this warp writes output columns ocol0 .. ocol0 + D/2 - 1
+      uint8_t* stage = gbase + kOffStage + warp * kStageBytes;
+      const int swz = (lane >> 1) & 3;
+      const int prow = lane >> 2, pj = lane & 3;  // copy-out: row within a group of 8, 16-byte unit
+      const bool f32_out = a.out_dtype == PA_F32;
+      const int esize = f32_out ? 4 : 2;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         float oa[32], ob[32];
@@ -823,31 +852,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         float o[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = c0w * oa[i] + c1w * ob[i];
-        if (store) {
-          if (a.out_dtype == PA_F32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + obase + cc * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + obase + cc * 32);
+        for (int ps = 0; ps < 2; ++ps) {  // 64-byte pieces: one for 16-bit outputs, two for fp32
+          if (ps == 1 && !f32_out) break;
+          uint4 v[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float* v = o + 8 * i;
-              uint4 w;
+          for (int j = 0; j < 4; ++j) {
+            if (f32_out) {
+              const float* f = o + 16 * ps + 4 * j;
+              v[j] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                                __float_as_uint(f[3]));
+            } else {
+              const float* f = o + 8 * j;
               if (a.out_dtype == PA_BF16) {
-                w.x = pack2<__nv_bfloat16>(v[0], v[1]);
-                w.y = pack2<__nv_bfloat16>(v[2], v[3]);
-                w.z = pack2<__nv_bfloat16>(v[4], v[5]);
-                w.w = pack2<__nv_bfloat16>(v[6], v[7]);
+                v[j] = make_uint4(pack2<__nv_bfloat16>(f[0], f[1]), pack2<__nv_bfloat16>(f[2], f[3]),
+                                  pack2<__nv_bfloat16>(f[4], f[5]), pack2<__nv_bfloat16>(f[6], f[7]));
               } else {
-                w.x = pack2<__half>(v[0], v[1]);
-                w.y = pack2<__half>(v[2], v[3]);
-                w.z = pack2<__half>(v[4], v[5]);
-                w.w = pack2<__half>(v[6], v[7]);
+                v[j] = make_uint4(pack2<__half>(f[0], f[1]), pack2<__half>(f[2], f[3]), pack2<__half>(f[4], f[5]),
+                                  pack2<__half>(f[6], f[7]));
               }
-              dst[i] = w;
+            }
+            *reinterpret_cast<uint4*>(stage + lane * 64 + ((j ^ swz) << 4)) = v[j];
+          }
+          __syncwarp();
+          const int col = ocol0 + cc * 32 + ps * 16;  // first output column of this piece
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int R = i * 8 + prow;
+            const uint4 w = *reinterpret_cast<const uint4*>(stage + R * 64 + ((pj ^ ((R >> 1) & 3)) << 4));
+            const int qr = it.row0 + quarter * 32 + R;
+            if (qr < it.n_c) {
+              uint8_t* dst = static_cast<uint8_t*>(a.out) +
+                             (((size_t)(it.q0 + qr) * H + it.h) * D + col) * esize + pj * 16;
+              *reinterpret_cast<uint4*>(dst) = w;
             }
           }
+          __syncwarp();
         }
       }
       // this warp is done with both accumulators and with xm / xl of this item

@@ -10,7 +10,12 @@
 //  * Persistent: one CTA per SM (its shared and tensor memory allow one),
 //    each walking a list of items -- (128-query tile, chunk, head) -- in
 //    longest-first order, 10 warps:
-//      warp 9  (loader)  TMA: per item the query tile (3-D tensor map over
+//      warp 9  (loader)  walks the item list and publishes each runnable
+//              item (its chunk, head, rows, context, key-tile count and
+//              whether every block-table entry it reads is in range) in a
+//              4-slot shared-memory ring that the other roles read, so that
+//              they do no lookups of their own between items;
+//              TMA: per item the query tile (3-D tensor map over
 //              [token][head][dim]) once the previous item's last S = Q K^T is
 //              done with the buffer; per 128-key tile the K rows and the V
 //              rows of its pages into 2- and 3-stage rings (2-D tensor maps
@@ -48,7 +53,9 @@
 //    in tensor memory); only then does the softmax of tile j wait for
 //    P_h(j-1) V, otherwise it overlaps it.  Ring stages and barrier phases
 //    follow running per-CTA counters, so the next item's query load and first
-//    two S products overlap the current item's last tiles and epilogue.
+//    two S products overlap the current item's last tiles and epilogue.  The
+//    output leaves through a 2 KB shared-memory slab per softmax warp, so
+//    that a store instruction writes 8 rows' 64-byte pieces.
 //  * Operands in shared memory are 128-byte swizzled: K-major for Q and K;
 //    V is consumed MN-major (dims contiguous), straight from the pool layout.
 //  * Keys past the context or in a bad page, and keys past a query's
@@ -101,7 +108,23 @@ constexpr uint32_t kOffStage = kOffV + kVStages * kTileBytes;
 constexpr uint32_t kOffBar = kOffStage + 8 * kStageBytes;
 constexpr int kPfRankMax = 1024;  // (chunk, query tile) pairs ranked in-kernel
 
+// An item as the loader publishes it to the MMA thread and the softmax warps.
+// The loader fills slot k % kItemSlots for its k-th runnable item after it has
+// issued V of the previous item's last key tile, which waits for the P V
+// product three tiles back; the softmax warps (and, ahead of them, the MMA
+// thread) copy a slot when they start its item, before any of the item's P.
+// Three tiles back lie at most three items back, so four slots are never
+// overwritten before they are read.
+constexpr int kItemSlots = 4;
+enum { kSlotNeedZero = 1, kSlotTableOk = 2, kSlotEnd = 4 };
+struct PfSlot {
+  int c, h, q0, n_c, row0, c0, ctx_total, n_kv;
+  int flags;  // kSlotNeedZero: the last key tile runs past the context; kSlotTableOk: every table
+              // entry the item reads is in range; kSlotEnd: no more items
+};
+
 struct PfBars {
+  uint64_t item_full[kItemSlots];  // the loader wrote the slot, one phase per use
   uint64_t q_full, q_empty;  // query tile loaded / its last S = Q K^T done
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
@@ -117,6 +140,7 @@ struct PfBars {
   float xl[2][kPfRows];  // half-row sum at the end: [half][row]
   int abort_flag;
   uint16_t order[kPfRankMax];  // (chunk, query tile) pairs, longest first
+  PfSlot items[kItemSlots];
 };
 constexpr uint32_t kPfSmemBytes = kOffBar + sizeof(PfBars) + 1024;  // + alignment slack
 static_assert(kPfSmemBytes <= 227 * 1024, "shared memory beyond the per-CTA limit");
@@ -435,6 +459,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
 
   if (threadIdx.x == 0) {
+    for (int i = 0; i < kItemSlots; ++i) mbar_init(&bars.item_full[i], 1);
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.q_empty, 1);
     for (int i = 0; i < kKStages; ++i) {
@@ -490,6 +515,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (st == kItemBadLength && lane == 0) atomicOr(a.err_flag, PA_FLAG_BAD_LENGTH);
       if (st != kItemRun) continue;
       const int32_t* trow = a.block_tables + (size_t)it.c * a.max_blocks_per_seq;
+      {  // publish the item, with whether every table entry it reads is in range
+        const int kend = min(it.ctx_total, it.n_kv * kPfKeys);
+        const int npages = (kend + B - 1) / B;
+        bool bad = false;
+#pragma unroll 4
+        for (int p = lane; p < npages; p += 32) {
+          const int32_t e = __ldg(trow + p);
+          bad |= (e < 0 || e >= a.num_blocks);
+        }
+        const bool table_ok = !__any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+          PfSlot& sl = bars.items[k % kItemSlots];
+          sl.c = it.c;
+          sl.h = it.h;
+          sl.q0 = it.q0;
+          sl.n_c = it.n_c;
+          sl.row0 = it.row0;
+          sl.c0 = it.c0;
+          sl.ctx_total = it.ctx_total;
+          sl.n_kv = it.n_kv;
+          sl.flags = (it.need_zero ? kSlotNeedZero : 0) | (table_ok ? kSlotTableOk : 0);
+          mbar_arrive(&bars.item_full[k % kItemSlots]);
+        }
+      }
       int wok = 1;
       if (lane == 0) {  // the query tile, once the previous item's last S = Q K^T is done with the buffer
         wok = mbar_wait(&bars.q_empty, (k & 1) ^ 1, abort_flag, a.err_flag);
@@ -561,6 +610,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       g += it.n_kv;
       ++k;
     }
+    if (ok && lane == 0) {  // the end of the list
+      bars.items[k % kItemSlots].flags = kSlotEnd;
+      mbar_arrive(&bars.item_full[k % kItemSlots]);
+    }
     if (lane == 0 && *abort_flag) {  // let in-flight copies land before exit
       if (k > 0) mbar_wait_drain(&bars.q_full, (k - 1) & 1);
       for (int x = max(0, k_issued - kKStages); x < k_issued; ++x)
@@ -572,14 +625,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
       const uint64_t qdesc = smem_desc_sw128(base + kOffQ, 16, 1024);
-      int g = 0, k = 0, nz = 0;
+      int g = 0, nz = 0;
       bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const long long ipos = pf_round_pos(r);
-        if (ipos >= n_items) break;
-        PfItem it;
-        if (pf_item(a, order, npairs, (int)ipos, it) != kItemRun) continue;
-        const int n_kv = it.n_kv;
+      for (int k = 0; ok; ++k) {
+        ok = mbar_wait(&bars.item_full[k % kItemSlots], (k / kItemSlots) & 1, abort_flag, a.err_flag);
+        if (!ok) break;
+        const int flags = bars.items[k % kItemSlots].flags;
+        if (flags & kSlotEnd) break;
+        const int n_kv = bars.items[k % kItemSlots].n_kv;
+        const bool need_zero = (flags & kSlotNeedZero) != 0;
         ok = mbar_wait(&bars.q_full, k & 1, abort_flag, a.err_flag);
         if (!ok) break;
         // S(x) = Q K_x^T into score buffer x % 2; after the item's last one the query buffer is free
@@ -605,7 +659,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int t = 0; ok && t < n_kv; ++t) {
           const int x = g + t;
           ok = mbar_wait(&bars.v_full[x % kVStages], (x / kVStages) & 1, abort_flag, a.err_flag);
-          if (ok && it.need_zero && t == n_kv - 1) ok = mbar_wait(&bars.v_zeroed, nz & 1, abort_flag, a.err_flag);
+          if (ok && need_zero && t == n_kv - 1) ok = mbar_wait(&bars.v_zeroed, nz & 1, abort_flag, a.err_flag);
           // the previous item's epilogue has read both output accumulators
           if (ok && t == 0) ok = mbar_wait(&bars.o_free, (k & 1) ^ 1, abort_flag, a.err_flag);
           const uint64_t vdesc = smem_desc_sw128(base + kOffV + (x % kVStages) * kTileBytes, kHalfBytes, 1024);
@@ -630,9 +684,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           umma_commit(&bars.v_empty[x % kVStages]);
           if (t + 2 < n_kv) ok = issue_s(t + 2);  // after P(x) V in issue order: its buffer is free then
         }
-        if (it.need_zero) ++nz;
+        if (need_zero) ++nz;
         g += n_kv;
-        ++k;
       }
       // every issued MMA has finished before tensor memory is released
       umma_commit(&bars.drain);
@@ -650,13 +703,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t o_mine = lane_addr + tmem_o(half);
     const int rpl = a.rows_per_load;
     const int pieces = kPfKeys / rpl;
-    int g = 0, k = 0;
+    int g = 0;
     bool ok = true;
-    for (int rr = 0; ok; ++rr) {
-      const long long ipos = pf_round_pos(rr);
-      if (ipos >= n_items) break;
+    for (int k = 0; ok; ++k) {
+      ok = mbar_wait(&bars.item_full[k % kItemSlots], (k / kItemSlots) & 1, abort_flag, a.err_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       PfItem it;
-      if (pf_item(a, order, npairs, (int)ipos, it) != kItemRun) continue;
+      bool all_ok;
+      {
+        const PfSlot& sl = bars.items[k % kItemSlots];
+        if (sl.flags & kSlotEnd) break;
+        it.c = sl.c;
+        it.h = sl.h;
+        it.q0 = sl.q0;
+        it.n_c = sl.n_c;
+        it.row0 = sl.row0;
+        it.c0 = sl.c0;
+        it.ctx_total = sl.ctx_total;
+        it.n_kv = sl.n_kv;
+        it.need_zero = (sl.flags & kSlotNeedZero) != 0;
+        all_ok = (sl.flags & kSlotTableOk) != 0;
+      }
       const int n_kv = it.n_kv;
       const int qrow = it.row0 + r;
       const int pos = it.c0 + qrow;
@@ -670,20 +740,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int p = t * kPfKeys + lane * rpl;
         return (t < n_kv && lane < pieces && p < ctx_total) ? __ldg(trow + p / B) : -1;
       };
-      // Every table entry the item reads in range: then no key tile needs a
-      // per-piece mask and the per-tile lookups are skipped.
-      bool all_ok;
-      {
-        const int kend = min(ctx_total, n_kv * kPfKeys);
-        const int npages = (kend + B - 1) / B;
-        bool bad = false;
-#pragma unroll 4
-        for (int p = lane; p < npages; p += 32) {
-          const int32_t e = __ldg(trow + p);
-          bad |= (e < 0 || e >= a.num_blocks);
-        }
-        all_ok = !__any_sync(0xffffffffu, bad);
-      }
+      // Every table entry the item reads in range (the loader checked): then
+      // no key tile needs a per-piece mask and the per-tile lookups are skipped.
       int32_t entry_next = all_ok ? 0 : piece_entry(0);
       float m_used = -INFINITY;
       float l = 0.f;
@@ -844,6 +902,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int prow = lane >> 2, pj = lane & 3;  // copy-out: row within a group of 8, 16-byte unit
       const bool f32_out = a.out_dtype == PA_F32;
       const int esize = f32_out ? 4 : 2;
+      const int wrow0 = it.row0 + quarter * 32;  // this warp's first row within the chunk
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         float oa[32], ob[32];
@@ -874,13 +933,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             *reinterpret_cast<uint4*>(stage + lane * 64 + ((j ^ swz) << 4)) = v[j];
           }
+          const int col = ocol0 + cc * 32 + (f32_out ? ps * 16 : 0);  // first output column of this piece
           __syncwarp();
-          const int col = ocol0 + cc * 32 + ps * 16;  // first output column of this piece
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int R = i * 8 + prow;
             const uint4 w = *reinterpret_cast<const uint4*>(stage + R * 64 + ((pj ^ ((R >> 1) & 3)) << 4));
-            const int qr = it.row0 + quarter * 32 + R;
+            const int qr = wrow0 + R;
             if (qr < it.n_c) {
               uint8_t* dst = static_cast<uint8_t*>(a.out) +
                              (((size_t)(it.q0 + qr) * H + it.h) * D + col) * esize + pj * 16;
@@ -895,7 +954,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.o_free);
       g += n_kv;
-      ++k;
     }
   }
   tc_fence_before();

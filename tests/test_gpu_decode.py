@@ -210,6 +210,15 @@ def test_decode_empty_context_and_bad_entries(pa):
     assert flags == pa.PA_FLAG_BAD_BLOCK
     assert torch.isfinite(out).all()
     assert_attn_close(out[:2], oracle_decode(w)[:2], "f32", "rows without a bad entry")
+    # sequence 2 (33 tokens, 16-token pages) without its second page: the
+    # oracle over the table with that entry taken out and 17 tokens
+    kept = w.block_tables.clone()
+    row = w.block_tables[2].tolist()
+    kept[2] = torch.tensor(row[:1] + row[2:] + row[:1], dtype=kept.dtype)
+    shorter = w.context_lens.clone()
+    shorter[2] = 17
+    ref = oracle_decode(w, ctx=shorter, tables=kept)
+    assert_attn_close(out[2:], ref[2:], "f32", "the row whose second page is out of range")
     too_long = w.context_lens.clone()
     too_long[1] = w.max_blocks_per_seq * w.block_size + 1
     out, flags = run_decode(pa, w, ctx=too_long, out_dtype="f32")

@@ -202,6 +202,33 @@ def test_prefill_flags_bad_table_entry(pa):
     assert torch.isfinite(out).all()
 
 
+@pytest.mark.parametrize("B,bad_page", [(16, 3), (48, 1)])
+def test_prefill_skips_the_keys_of_a_bad_page(pa, B, bad_page):
+    """Keys in a page whose table entry is out of range are skipped, and the
+    call flags it.  The reference is the oracle over the sequence with that
+    page's entry taken out of the table: there row p sits at p (before the
+    page), at the page's first position minus one (inside it) or at p - B
+    (after it); each row runs as a one-row chunk at that position."""
+    m = W.small_prefill(chunk_lens=(300,), ctx_before=(0,), H=2, B=B)
+    w = m.decode
+    bad = m.chunk_tables.clone()
+    bad[0, bad_page] = -3
+    out, flags, _, _ = run_prefill(pa, m, "f32", tables=bad)
+    assert flags == pa.PA_FLAG_BAD_BLOCK
+
+    kb, vb = oracle.pool_bits(w.k_pool), oracle.pool_bits(w.v_pool)
+    seq_idx, pos = chunk_positions(m)
+    oracle.reshape_and_cache(m.chunk_k, m.chunk_v, kb, vb, oracle_slots(m.chunk_tables, seq_idx, pos, B), B)
+    row = m.chunk_tables[0].tolist()
+    kept = row[:bad_page] + row[bad_page + 1:] + [row[0]]
+    T = int(m.chunk_lens[0])
+    lo, hi = bad_page * B, (bad_page + 1) * B
+    at = [p if p < lo else (lo - 1 if p < hi else p - B) for p in range(T)]
+    ref = oracle.prefill(m.chunk_q, torch.arange(T + 1, dtype=torch.int32), torch.tensor(at, dtype=torch.int32), kb,
+                         vb, torch.tensor([kept] * T, dtype=torch.int32), B, w.scale, w.dtype)
+    assert_attn_close(out, ref, "f32", f"prefill, page {bad_page} of {B} tokens out of range")
+
+
 def test_prefill_many_items_per_cta(pa):
     """Ten or so (query tile, head) items per CTA of the persistent grid, with
     an empty chunk and chunks of one row among them: every item's output must

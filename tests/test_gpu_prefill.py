@@ -33,12 +33,13 @@ def cu_lens(m):
     return torch.cat([torch.zeros(1, dtype=torch.int32), m.chunk_lens.cumsum(0).to(torch.int32)])
 
 
-def run_prefill(pa, m, out_dtype="f32", tables=None):
+def run_prefill(pa, m, out_dtype="f32", tables=None, ctx_before=None):
     """Write the chunks' K/V with pa_reshape_and_cache, then pa_prefill_chunk."""
     w = m.decode
     dev = torch.device("cuda")
     kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
     tables = m.chunk_tables if tables is None else tables
+    ctx_before = m.ctx_before if ctx_before is None else ctx_before
     seq_idx, pos = chunk_positions(m)
     slots = pa.pa_slot_mapping(m.chunk_tables, seq_idx, pos, w.block_size)
     err = pa.new_error_flag()
@@ -46,7 +47,7 @@ def run_prefill(pa, m, out_dtype="f32", tables=None):
     assert pa.pa_get_error(err) == 0
     T = int(m.chunk_lens.sum())
     out = torch.full((T, w.num_heads, w.head_dim), float("nan"), dtype=TORCH_OUT[out_dtype], device=dev)
-    pa.pa_prefill_chunk(out, m.chunk_q.to(dev), cu_lens(m).to(dev), m.ctx_before.to(dev), kp, vp, tables.to(dev),
+    pa.pa_prefill_chunk(out, m.chunk_q.to(dev), cu_lens(m).to(dev), ctx_before.to(dev), kp, vp, tables.to(dev),
                         int(m.chunk_lens.max()), w.scale, err)
     flags = pa.pa_get_error(err)
     return out, flags, kp, vp
@@ -227,6 +228,30 @@ def test_prefill_skips_the_keys_of_a_bad_page(pa, B, bad_page):
     ref = oracle.prefill(m.chunk_q, torch.arange(T + 1, dtype=torch.int32), torch.tensor(at, dtype=torch.int32), kb,
                          vb, torch.tensor([kept] * T, dtype=torch.int32), B, w.scale, w.dtype)
     assert_attn_close(out, ref, "f32", f"prefill, page {bad_page} of {B} tokens out of range")
+
+
+def test_prefill_skips_a_chunk_whose_context_overruns_its_table(pa):
+    """A chunk whose last position lies past its table's capacity is flagged
+    and skipped (its output rows are not written); the chunks beside it are
+    computed as usual."""
+    m = W.small_prefill(chunk_lens=(100, 50, 80), ctx_before=(10, 20, 30), H=2, B=16)
+    cb = m.ctx_before.clone()
+    cb[1] = m.chunk_tables.shape[1] * 16
+    out, flags, _, _ = run_prefill(pa, m, "f32", ctx_before=cb)
+    assert flags == pa.PA_FLAG_BAD_LENGTH
+    assert torch.isnan(out[100:150]).all()
+    keep = torch.cat([torch.arange(0, 100), torch.arange(150, 230)])
+    ref, _, _ = oracle_prefill(m)
+    assert_attn_close(out[keep.cuda()], ref[keep.numpy()], "f32", "chunks beside the skipped one")
+
+
+def test_prefill_with_every_chunk_skipped_ends_cleanly(pa):
+    """No runnable item at all: every CTA sees only the end of the list."""
+    m = W.small_prefill(chunk_lens=(40, 9), ctx_before=(0, 0), H=2, B=16)
+    cb = torch.full_like(m.ctx_before, m.chunk_tables.shape[1] * 16)
+    out, flags, _, _ = run_prefill(pa, m, "bf16", ctx_before=cb)
+    assert flags == pa.PA_FLAG_BAD_LENGTH
+    assert torch.isnan(out.float()).all()
 
 
 def test_prefill_many_items_per_cta(pa):

@@ -498,9 +498,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   volatile int* abort_flag = &bars.abort_flag;
   const uint16_t* order = bars.order;
 
-  // Every role walks the same item list.  Ring stages and barrier phases
-  // follow running counters: g = key tiles of this CTA's earlier items (the
-  // global index of a key tile is g + t), k = items run so far.
+  // The loader walks this CTA's items and publishes each runnable one; the
+  // MMA thread and the softmax warps take them from the item ring in the same
+  // order.  Ring stages and barrier phases follow running counters: g = key
+  // tiles of this CTA's earlier items (the global index of a key tile is
+  // g + t), k = items run so far.
   if (warp == kPfLoadWarp) {
     // ---------------------------------------------------------------- loader
     const int rpl = a.rows_per_load;

@@ -67,6 +67,43 @@ def test_decode_random_cases(pa, case):
     assert_attn_close(out, ref, out_dtype, f"case {case}: S={S} H={H} D={D} B={B} {dtype} P={P} ctx={ctx.tolist()}")
 
 
+@pytest.mark.parametrize("case", range(10))
+def test_decode_random_cases_with_a_bad_page(pa, case):
+    """One table entry of one sequence out of range: the call flags it and the
+    sequence's output is the oracle over the same sequence without that page
+    (its entry taken out of the table, its context shorter by the page's
+    tokens); the other sequences are unaffected."""
+    rng = np.random.default_rng(3000 + case)
+    D = int(rng.choice([64, 128]))
+    B = int(rng.choice([16, 32, 48, 64]))
+    H = int(rng.integers(1, 4))
+    S = int(rng.integers(2, 6))
+    dtype = str(rng.choice(["f16", "bf16"]))
+    P = int(rng.choice([0, 16, 64, 512]))
+    ctx = torch.tensor([int(rng.integers(B + 1, 900)) for _ in range(S)], dtype=torch.int32)
+    w = W._decode_workload(f"badpage{case}", ctx, ctx - 1, H, D, B, dtype, seed=90 + case)
+    s_bad = int(rng.integers(0, S))
+    n_pages = (int(ctx[s_bad]) + B - 1) // B
+    j = int(rng.integers(0, n_pages))
+    tables = w.block_tables.clone()
+    tables[s_bad, j] = w.num_blocks + int(rng.integers(0, 5))
+    dev = torch.device("cuda")
+    mx = int(ctx.max())
+    out = torch.full((S, H, D), float("nan"), dtype=torch.float32, device=dev)
+    ws = pa.decode_workspace(S, H, D, mx, P)
+    err = pa.new_error_flag()
+    pa.pa_decode(out, w.q.to(dev), w.k_pool.to(dev), w.v_pool.to(dev), tables.to(dev), ctx.to(dev), mx, w.scale, ws,
+                 err, partition_size=P)
+    assert pa.pa_get_error(err) == pa.PA_FLAG_BAD_BLOCK
+    kept = w.block_tables.clone()
+    row = w.block_tables[s_bad].tolist()
+    kept[s_bad] = torch.tensor(row[:j] + row[j + 1:] + row[:1], dtype=kept.dtype)
+    shorter = ctx.clone()
+    shorter[s_bad] = int(ctx[s_bad]) - (min((j + 1) * B, int(ctx[s_bad])) - j * B)
+    ref = oracle.decode(w.q, w.k_pool, w.v_pool, kept, shorter, B, w.scale, dtype)
+    assert_attn_close(out, ref, "f32", f"case {case}: S={S} H={H} D={D} B={B} {dtype} P={P} bad page {j} of seq {s_bad}")
+
+
 @pytest.mark.parametrize("case", range(N_PREFILL))
 def test_prefill_random_cases(pa, case):
     rng = np.random.default_rng(2000 + case)

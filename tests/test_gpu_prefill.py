@@ -203,14 +203,15 @@ def test_prefill_flags_bad_table_entry(pa):
     assert torch.isfinite(out).all()
 
 
-@pytest.mark.parametrize("B,bad_page", [(16, 3), (48, 1)])
-def test_prefill_skips_the_keys_of_a_bad_page(pa, B, bad_page):
+@pytest.mark.parametrize("B,bad_page,dtype,D", [(16, 3, "bf16", 128), (48, 1, "bf16", 128), (16, 2, "f16", 64),
+                                               (32, 5, "f16", 128)])
+def test_prefill_skips_the_keys_of_a_bad_page(pa, B, bad_page, dtype, D):
     """Keys in a page whose table entry is out of range are skipped, and the
     call flags it.  The reference is the oracle over the sequence with that
     page's entry taken out of the table: there row p sits at p (before the
     page), at the page's first position minus one (inside it) or at p - B
     (after it); each row runs as a one-row chunk at that position."""
-    m = W.small_prefill(chunk_lens=(300,), ctx_before=(0,), H=2, B=B)
+    m = W.small_prefill(chunk_lens=(300,), ctx_before=(0,), H=2, B=B, D=D, dtype=dtype)
     w = m.decode
     bad = m.chunk_tables.clone()
     bad[0, bad_page] = -3

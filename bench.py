@@ -48,9 +48,17 @@ TRAFFIC = {"bytes_per_launch": 1488338856, "kernel_sha256_prefix": "a53b700b600e
            "source": "profiles/decode_kernel_llama13b_b64.md"}
 
 
-def kernel_sha() -> str:
+# DRAM bytes (read + write) per pa_prefill_chunk call on the four-prompt
+# prefill workloads, from the ncu captures summarised in profiles/; valid only
+# for the prefill kernel source whose sha256 prefix is given.
+PREFILL_TRAFFIC = {"kernel_sha256_prefix": "f8e98b7cdf614604",
+                   "bf16": {"bytes_per_launch": 1225448192, "source": "profiles/prefill_kernel_4x2048.md"},
+                   "f16": {"bytes_per_launch": 1230640128, "source": "profiles/prefill_kernel_4x2048_f16.md"}}
+
+
+def kernel_sha(files=("pa_decode.cu", "pa_common.cuh")) -> str:
     h = hashlib.sha256()
-    for f in ("pa_decode.cu", "pa_common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_cache_35_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -788,6 +796,9 @@ def run_prefill(args, rank, world, local):
         raise RuntimeError("device error flags in the end-to-end pass")
 
     peak, peak_kind = load_tensor_peak()
+    pf_sha = kernel_sha(("pa_prefill.cu", "pa_common.cuh"))
+    pf_traffic = (PREFILL_TRAFFIC[dtype]["bytes_per_launch"] if PREFILL_TRAFFIC["kernel_sha256_prefix"] == pf_sha
+                  else None)
     pre_avg_s = statistics.mean(pre_ms) / 1e3
     achieved = flops / pre_avg_s / 1e12
     line = {
@@ -800,12 +811,12 @@ def run_prefill(args, rank, world, local):
                          "writes it to the pool, the prefill reads it and 84 MB of queries and writes 84 MB)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak, "traffic": pf_traffic, "peak_kind": peak_kind,
                      "kernel": "prefill_kernel (pa_prefill_chunk)", "algorithmic_flops_per_launch": flops,
                      "avg_launch_ms": pre_avg_s * 1e3, "timed_calls": len(pre_ms),
                      "tensor_flops_executed_per_launch": flops * (3 if dtype == "bf16" else 2) // 2,
-                     "note": "bf16: P V runs as two products (P_hi, P_lo); fp16: one. DRAM traffic of one "
-                             "bf16 launch: profiles/prefill_kernel_4x2048.md"},
+                     "kernel_sha256_prefix": pf_sha, "traffic_source": PREFILL_TRAFFIC[dtype]["source"],
+                     "note": "bf16: P V runs as two products (P_hi, P_lo); fp16: one"},
         "e2e": {"value": flops * Ke * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / Ke, "steps": Ke,
                 "overlap": "copies on their own streams, double-buffered, overlapping the previous step"},

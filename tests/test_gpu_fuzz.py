@@ -15,8 +15,8 @@ from tests.gpu_common import TORCH_OUT, assert_attn_close, oracle_slots
 
 pytestmark = pytest.mark.gpu
 
-N_DECODE = 40
-N_PREFILL = 40
+N_DECODE = 100
+N_PREFILL = 100
 
 
 @pytest.fixture(scope="module")

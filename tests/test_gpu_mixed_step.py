@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import pa_workloads as W
-from tests.gpu_common import assert_attn_close, oracle_slots
+from tests.gpu_common import assert_attn_close, bits_equal, oracle_slots
 
 pytestmark = pytest.mark.gpu
 
@@ -118,15 +118,13 @@ def test_mixed_step_budget512_matches_oracle(pa):
                               oracle_slots(m.chunk_tables, st.seq_idx, st.pos, w.block_size)])
     oracle.reshape_and_cache(torch.cat([host["k_new"], chunk_k]), torch.cat([host["v_new"], chunk_v]), kb, vb,
                              o_slots, w.block_size)
+    assert bits_equal(w.k_pool, kb) and bits_equal(w.v_pool, vb)
     dref = oracle.decode(host["q"], kb, vb, w.block_tables, w.context_lens, w.block_size, w.scale, "bf16")
     assert_attn_close(d_host, dref, "bf16", "budget-512 step: decode part")
-    rows = torch.unique(torch.cat([torch.arange(0, 480, 7), torch.tensor([0, 127, 128, 479])]))
-    c0 = int(m.ctx_before[0])
-    sub_cb = (c0 + rows).to(torch.int32)
-    sub_cu = torch.arange(len(rows) + 1, dtype=torch.int32)
-    sub_tables = m.chunk_tables[torch.zeros(len(rows), dtype=torch.long)]
-    pref = oracle.prefill(chunk_q[rows], sub_cu, sub_cb, kb, vb, sub_tables, w.block_size, w.scale, "bf16")
-    assert_attn_close(p_host[rows], pref, "bf16", "budget-512 step: prefill part")
+    # every row of the 480-query chunk
+    cu = torch.cat([torch.zeros(1, dtype=torch.int32), m.chunk_lens.cpu().cumsum(0).to(torch.int32)])
+    pref = oracle.prefill(chunk_q, cu, m.ctx_before.cpu(), kb, vb, m.chunk_tables, w.block_size, w.scale, "bf16")
+    assert_attn_close(p_host, pref, "bf16", "budget-512 step: prefill part")
 
 
 def test_mixed_step_refuses_bad_arguments_before_launching(pa):

@@ -2,7 +2,10 @@
 of request A's.  With the allocator's prefix cache, B takes over A's five
 completed blocks and only its 30 new tokens are scattered and prefilled
 (ctx_before = 80).  The rows must equal, bit for bit, those of the same
-request prefilled in full without the cache, and match the oracle."""
+request prefilled in full without the cache, and match the oracle.  The
+oracle side replays both requests through the allocator model and its own
+scalar scatter, starting from zeroed pools: the tables must agree with the
+C++ allocator's and the GPU's pools with the oracle's, bit for bit."""
 from __future__ import annotations
 
 import numpy as np
@@ -11,7 +14,8 @@ import torch
 
 import oracle
 import pa_workloads as W
-from tests.gpu_common import assert_attn_close, oracle_slots
+from oracle.alloc_model import BlockAllocatorModel
+from tests.gpu_common import assert_attn_close
 
 pytestmark = pytest.mark.gpu
 
@@ -81,8 +85,24 @@ def test_second_request_reuses_the_cached_prefix(pa):
     assert n0 == 0
     assert torch.equal(out_b, full[80:])
 
-    # oracle: B's full context through its (shared) table
-    kbits, vbits = oracle.pool_bits(kp.cpu()), oracle.pool_bits(vp.cpu())
+    # oracle: both requests replayed through the allocator model and the
+    # oracle's scatter into zeroed pools of its own
+    model = BlockAllocatorModel(NB, B, prefix_cache=True)
+    kbits = np.zeros((NB, H, B, D), dtype=np.uint16)
+    vbits = np.zeros_like(kbits)
+    for seq, prompt, (k_all, v_all, _) in ((0, prompt_a, kv_a), (1, prompt_b, kv_b)):
+        n0 = model.add_seq_prefix(seq, prompt)
+        new = list(range(n0, len(prompt)))
+        slots = []
+        for p in new:
+            sl, pairs = model.append_slots([seq], [prompt[p]])
+            assert pairs == []
+            slots.append(sl[0])
+        oracle.reshape_and_cache(k_all[new], v_all[new], kbits, vbits, np.array(slots, dtype=np.int64), B)
+    model_table = torch.full((1, 16), -1, dtype=torch.int32)
+    model_table[0, : len(model.table(1))] = torch.tensor(model.table(1), dtype=torch.int32)
+    assert torch.equal(model_table, table_b)
+    assert np.array_equal(oracle.pool_bits(kp.cpu()), kbits) and np.array_equal(oracle.pool_bits(vp.cpu()), vbits)
     ref = oracle.prefill(kv_b[2][80:], torch.tensor([0, 30], dtype=torch.int32), torch.tensor([80], dtype=torch.int32),
-                         kbits, vbits, table_b, B, 1 / np.sqrt(D), "bf16")
+                         kbits, vbits, model_table, B, 1 / np.sqrt(D), "bf16")
     assert_attn_close(out_b, ref, "f32", "prefix-cached prefill")

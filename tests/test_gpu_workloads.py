@@ -4,13 +4,17 @@ benchmark times:
 * LLaMA-13B-shaped decode: 64 sequences x 40 heads x 128, block 16,
   contexts uniform in [128, 2048], fp16 (every (sequence, head) checked);
 * long-context decode: 256 sequences x 32 heads, bf16, log-normal contexts
-  up to 16384 (every 4th sequence checked against the oracle, every output
-  checked finite);
+  up to 16384 (every sequence checked against the oracle);
 * parallel sampling with a shared 1000-token prompt: host allocator,
   copy-on-write pairs, block copy, scatter and decode, replayed on the oracle
   side with its own allocator model;
 * mixed chunked prefill: 32 decode sequences plus two 512-token chunks at
-  contexts 1024 and 3072, page size 256, bf16.
+  contexts 1024 and 3072, page size 256, bf16 (every decode sequence and
+  every chunk row checked).
+
+The oracle's pools always come from its own scatter (and, for parallel
+sampling, its own copies) of host copies of the inputs; the GPU's pools
+must equal them bit for bit.
 """
 from __future__ import annotations
 
@@ -69,7 +73,9 @@ def test_llama13b_decode_full(pa):
     assert_attn_close(out, ref, "f16", "llama13b decode")
 
 
-def test_long_context_decode_sampled(pa):
+def test_long_context_decode_full(pa):
+    """All 256 sequences of the long-context batch (log-normal contexts up
+    to 16384, split-KV partitions merged in-kernel) against the oracle."""
     w = W.long_context_decode(device="cuda")
     host = _host_copy(w)
     out = decode_step(pa, w, out_dtype=torch.bfloat16)
@@ -77,12 +83,9 @@ def test_long_context_decode_sampled(pa):
     kb, vb = oracle.pool_bits(host["k_pool"]), oracle.pool_bits(host["v_pool"])
     oracle.reshape_and_cache(host["k_new"], host["v_new"], kb, vb,
                              oracle_slots(w.block_tables, range(w.num_seqs), w.new_pos, w.block_size), w.block_size)
-    rows = torch.arange(0, w.num_seqs, 4)
-    longest = int(torch.argmax(w.context_lens))
-    rows = torch.unique(torch.cat([rows, torch.tensor([longest])]))
-    ref = oracle.decode(host["q"][rows], kb, vb, w.block_tables[rows], w.context_lens[rows], w.block_size, w.scale,
-                        "bf16")
-    assert_attn_close(out[rows.cuda()], ref, "bf16", "long-context decode")
+    assert bits_equal(w.k_pool, kb) and bits_equal(w.v_pool, vb)
+    ref = oracle.decode(host["q"], kb, vb, w.block_tables, w.context_lens, w.block_size, w.scale, "bf16")
+    assert_attn_close(out, ref, "bf16", "long-context decode")
 
 
 def test_shared_prefix_parallel_sampling(pa):
@@ -200,12 +203,6 @@ def test_mixed_chunked_prefill_full(pa):
     assert bits_equal(w.k_pool, kb) and bits_equal(w.v_pool, vb)
     dref = oracle.decode(host["q"], kb, vb, w.block_tables, w.context_lens, w.block_size, w.scale, "bf16")
     assert_attn_close(dout, dref, "bf16", "mixed: decode part")
-    rows = torch.cat([torch.arange(0, 512, 9), torch.arange(512, 1024, 9), torch.tensor([511, 1023])])
-    rows = torch.unique(rows)
-    # the oracle computes the chunk rows it is given: pass them as 1-row chunks
-    sub_q = chunk_q[rows]
-    sub_cb = torch.tensor([int(m.ctx_before[int(r) // 512]) + int(r) % 512 for r in rows], dtype=torch.int32)
-    sub_cu = torch.arange(len(rows) + 1, dtype=torch.int32)
-    sub_tables = m.chunk_tables[(rows // 512).long()]
-    pref = oracle.prefill(sub_q, sub_cu, sub_cb, kb, vb, sub_tables, w.block_size, w.scale, "bf16")
-    assert_attn_close(pout[rows.cuda()], pref, "bf16", "mixed: prefill part")
+    # every row of both chunks
+    pref = oracle.prefill(chunk_q, cu, m.ctx_before.cpu(), kb, vb, m.chunk_tables, w.block_size, w.scale, "bf16")
+    assert_attn_close(pout, pref, "bf16", "mixed: prefill part")

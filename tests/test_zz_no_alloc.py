@@ -9,9 +9,12 @@ pa_decode but keeps its scratch in a fixed device array inside the library.
 
 These tests call it through the C ABI and check its output against
 pa_decode with a caller-allocated workspace, on two different calls in a
-row (the array keeps whatever the previous call left in it), and check that
-a request larger than the fixed array is refused without a launch.  This
-file is collected last so that a failure here comes after every other test.
+row (the array keeps whatever the previous call left in it).  Both run the
+same deterministic kernels on the same inputs, so the outputs must be equal
+bit for bit; each call is also checked against the fp64 oracle within the
+attention tolerance of the other parity tests.  A request larger than the
+fixed array must be refused without a launch.  This file is collected last
+so that a failure here comes after every other test.
 """
 from __future__ import annotations
 
@@ -20,11 +23,13 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import pa_workloads as W
+from tests.gpu_common import assert_attn_close
 
 pytestmark = pytest.mark.gpu
 
-GATE = 2e-3  # the attention tolerance the other parity tests use
+OUT_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}
 
 
 @pytest.fixture(scope="module")
@@ -67,8 +72,11 @@ def _compare_one(pa, w, partition_size, out_dtype):
     st = _static_call(pa, got, q, kp, vp, tables, ctx, mx, w.scale, err, partition_size)
     assert st == pa.PA_OK, pa.status_string(st)
     assert pa.pa_get_error(err) == 0
-    diff = (got.float() - ref.float()).abs().max().item()
-    assert diff <= GATE, diff
+    assert torch.equal(got.view(torch.uint8), ref.view(torch.uint8))
+    # and the fp64 oracle over the same pools
+    kb, vb = oracle.pool_bits(kp.cpu()), oracle.pool_bits(vp.cpu())
+    expect = oracle.decode(w.q.cpu(), kb, vb, w.block_tables, w.context_lens, w.block_size, w.scale, w.dtype)
+    assert_attn_close(got, expect, OUT_NAME[out_dtype], "static-scratch decode")
 
 
 def test_static_scratch_matches_pa_decode_on_two_calls_in_a_row(pa):

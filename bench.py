@@ -41,19 +41,18 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and seq-steps/sec"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) per pa_decode call on this workload, from the ncu
-# capture summarised in profiles/; valid only for the decode kernel source
-# whose sha256 prefix is given (otherwise reported as null).
-TRAFFIC = {"bytes_per_launch": 1488338856, "kernel_sha256_prefix": "a53b700b600e6a63",
-           "source": "profiles/decode_kernel_llama13b_b64.md"}
+# DRAM bytes (read + write) per pa_decode call on the LLaMA-13B-shaped
+# workload, from an ncu capture of one launch (dram__bytes_read.sum +
+# dram__bytes_write.sum); valid only for the decode kernel source whose
+# sha256 prefix is given (otherwise reported as null).
+TRAFFIC = {"bytes_per_launch": 1488338856, "kernel_sha256_prefix": "a53b700b600e6a63"}
 
 
 # DRAM bytes (read + write) per pa_prefill_chunk call on the four-prompt
-# prefill workloads, from the ncu captures summarised in profiles/; valid only
-# for the prefill kernel source whose sha256 prefix is given.
+# prefill workloads, from ncu captures of one launch each; valid only for the
+# prefill kernel source whose sha256 prefix is given.
 PREFILL_TRAFFIC = {"kernel_sha256_prefix": "f8e98b7cdf614604",
-                   "bf16": {"bytes_per_launch": 1225448192, "source": "profiles/prefill_kernel_4x2048.md"},
-                   "f16": {"bytes_per_launch": 1230640128, "source": "profiles/prefill_kernel_4x2048_f16.md"}}
+                   "bf16": {"bytes_per_launch": 1225448192}, "f16": {"bytes_per_launch": 1230640128}}
 
 
 def kernel_sha(files=("pa_decode.cu", "pa_common.cuh")) -> str:
@@ -110,17 +109,99 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+class NvmlPoller:
+    """Reads the SM clock and the clock-event reasons of one GPU through NVML
+    (ctypes on the driver's libnvidia-ml, read-only calls) every `period_s`
+    in a thread, so that a timed region shorter than nvidia-smi's sampling
+    period still gets samples of its own."""
+
+    SW_POWER_CAP, HW_SLOWDOWN, SW_THERMAL, HW_THERMAL, HW_POWER_BRAKE = 0x4, 0x8, 0x20, 0x40, 0x80
+
+    def __init__(self, pci_bus_id, index: int, period_s: float = 0.002):
+        import ctypes
+
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            rc = -1
+            if pci_bus_id:
+                rc = nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h))
+            if rc != 0:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h))
+            if rc != 0:
+                return
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+            self.nv, self.h, self.ctypes = nv, h, ctypes
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def start(self):
+        if self.ok:
+            threading.Thread(target=self._run, daemon=True).start()
+
+    def _run(self):
+        ct = self.ctypes
+        clk, rsn = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0 and \
+                    self.reasons_fn(self.h, ct.byref(rsn)) == 0:
+                self.samples.append((time.time(), float(clk.value), int(rsn.value)))
+            time.sleep(self.period)
+
+    def stop(self):
+        self._stop.set()
+
+    def summary(self, t0, t1):
+        inside = [(c, r) for t, c, r in self.samples if t0 <= t <= t1]
+        if not inside:
+            return None
+        names = {self.SW_POWER_CAP: "sw_power_cap", self.HW_SLOWDOWN: "hw_slowdown",
+                 self.SW_THERMAL: "sw_thermal_slowdown", self.HW_THERMAL: "hw_thermal_slowdown",
+                 self.HW_POWER_BRAKE: "hw_power_brake_slowdown"}
+        reasons = sorted({n for c, r in inside for bit, n in names.items() if r & bit})
+        mhz = [c for c, _ in inside]
+        return {"sm_mhz": statistics.median(mhz), "sm_mhz_min": min(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def _pci_bus_id(gpu_index: int):
+    try:
+        import torch
+
+        p = torch.cuda.get_device_properties(gpu_index)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        return None
+
+
 class ClockSampler:
+    """nvidia-smi's clock line every 100 ms (the recipe's fields) and an NVML
+    poll every 2 ms, over the same GPU (found by its PCI bus id)."""
+
     def __init__(self, gpu_index: int):
         self.samples = []
         self.proc = None
         self.gpu = gpu_index
+        self.bus = _pci_bus_id(gpu_index)
+        self.nvml = NvmlPoller(self.bus, gpu_index)
 
     def start(self):
+        self.nvml.start()
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", f"--id={self.bus or self.gpu}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
@@ -131,6 +212,7 @@ class ClockSampler:
             self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
 
     def stop(self):
+        self.nvml.stop()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -139,25 +221,36 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
+        fast = self.nvml.summary(t0, t1)
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        inside = [s for t, s in self.samples if t0 <= t <= t1]
-        window = "timed region"
-        if not inside:
-            inside = [s for _, s in self.samples]
-            window = "whole run (timed region shorter than the sampling period)"
-        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
-        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for s in inside:
-            for n, v in zip(names, s[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        pw = [float(s[3]) for s in inside if s[3].replace(".", "").isdigit()]
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "power_w_max": max(pw) if pw else None, "samples": len(inside),
-                "window": window}
+            res = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        else:
+            inside = [s for t, s in self.samples if t0 <= t <= t1]
+            window = "timed region"
+            if not inside:
+                inside = [s for _, s in self.samples]
+                window = "whole run (timed region shorter than the sampling period)"
+            sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+            mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+            reasons = set()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for s in inside:
+                for n, v in zip(names, s[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            pw = [float(s[3]) for s in inside if s[3].replace(".", "").isdigit()]
+            res = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                   "reasons": sorted(reasons), "power_w_max": max(pw) if pw else None, "samples": len(inside),
+                   "window": window}
+        if fast is not None:
+            # the 2 ms poll covers the timed region itself: it sets the headline clock figures
+            res["nvidia_smi"] = {k: res[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "window")
+                                 if k in res}
+            res.update({"sm_mhz": fast["sm_mhz"], "sm_mhz_min": fast["sm_mhz_min"],
+                        "sm_max_mhz": fast["sm_max_mhz"] or res.get("sm_max_mhz"),
+                        "reasons": sorted(set(fast["reasons"]) | set(res.get("reasons", [])) - {"nvidia-smi unavailable"}),
+                        "samples": fast["samples"], "window": "timed region (NVML poll every 2 ms)"})
+        return res
 
 
 # ---- distributed plumbing ------------------------------------------------------------------------
@@ -364,6 +457,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config("llama13b", w),
+        "parallelism": "none: the CPU oracle on the host cores of rank 0",
         "seq_steps_per_s": nsub * args.steps / el,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": sample},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -372,24 +466,87 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local):
+def time_calls(fn, stream, dev, n_back: int, n_each: int) -> dict:
+    """Device time of one call of `fn` on `stream`: `n_back` calls back to
+    back between two events (the mean, which the rooflines use), then
+    `n_each` calls each between events of its own (median, min and max; an
+    event recorded between two kernels stops the next one's programmatic
+    early start, so these run slightly longer than the back-to-back mean)."""
+    import torch
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    a, b = ev(), ev()
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(n_back):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    mean_ms = a.elapsed_time(b) / n_back
+    s, e = [ev() for _ in range(n_each)], [ev() for _ in range(n_each)]
+    for i in range(n_each):
+        s[i].record(stream)
+        fn()
+        e[i].record(stream)
+    torch.cuda.synchronize(dev)
+    per = sorted(x.elapsed_time(y) for x, y in zip(s, e))
+    return {"mean_ms_back_to_back": mean_ms, "calls_back_to_back": n_back, "median_ms": statistics.median(per),
+            "min_ms": per[0], "max_ms": per[-1], "calls_timed_each": n_each}
+
+
+def call_stats(per_ms) -> dict:
+    per = sorted(per_ms)
+    return {"mean_ms": statistics.mean(per), "median_ms": statistics.median(per), "min_ms": per[0],
+            "max_ms": per[-1], "calls_timed_each": len(per)}
+
+
+def cpu_baseline_decode(w, budget_s: float, elt: int = 2) -> dict:
+    """The oracle (scatter + decode) timed on the host cores with its OpenMP
+    loops on every core, and single-threaded on the first sequences (a
+    bounded sample of the same workload); the same GB/s unit as the line."""
+    import oracle
+
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    host = {k: getattr(w, k).cpu() for k in ("k_pool", "v_pool", "q", "k_new", "v_new")}
+    thr = oracle.num_threads()
+    full = OracleStep(w, host)
+    t_rep, reps = full.time(budget_s)
+    res = {"value": (decode_bytes(w.context_lens.tolist(), H, D, B, elt) + scatter_bytes(w.num_seqs, H, D, elt))
+           / t_rep / 1e9, "unit": "GB/s", "cores": thr, "kind": "oracle",
+           "sample": f"the whole step's scatter + decode on {thr} threads (OpenMP over (sequence, head)), "
+                     f"{reps} repetitions, {t_rep * reps:.1f} s wall"}
+    nsub = max(1, min(w.num_seqs, 8))
+    sub = OracleStep(w, host, rows=range(nsub))
+    oracle.set_num_threads(1)
+    try:
+        t1, r1 = sub.time(budget_s / 2)
+    finally:
+        oracle.set_num_threads(thr)
+    sub_b = decode_bytes(sub.ctx.tolist(), H, D, B, elt) + scatter_bytes(nsub, H, D, elt)
+    res["single_thread"] = {"value": sub_b / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": f"scatter + decode of the first {nsub} of {w.num_seqs} sequences, one "
+                                      f"thread, {r1} repetitions, {t1 * r1:.1f} s wall"}
+    return res
+
+
+def measure_decode(args, rank, world, local, name, secondary=False):
+    """One decode-path workload: warm-up, K timed steps, then the kernel
+    timings for the roofline.  `secondary` (the other configurations of the
+    default run) skips the end-to-end pass, the CPU baseline and the graph
+    comparison.  Returns the JSON line as a dict."""
     import numpy as np
     import torch
 
-    import __graft_entry__
-
-    __graft_entry__.build()
     import paged_kv_cache_35_gb300 as pa
     import pa_workloads as W
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    name = args.workload
     mixed = None
     if name == "llama13b":
         w = W.llama13b_decode(device=dev)
     elif name == "long_context":
-        w = W.long_context_decode(device=dev)
+        w = W.long_context_decode(device=dev, num_seqs=args.num_seqs or 256)
     elif name == "tiny":
         w = W.tiny_decode(device=dev)
     elif name == "shared_prefix":
@@ -462,13 +619,46 @@ def run_ours(args, rank, world, local):
 
     K = args.steps
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    seq_ms = None
-    if mixed is not None:
-        # Component pass (untimed for the headline): each kernel alone, per-call
-        # events, for the rooflines -- inside the concurrent step the decode's
-        # events would also span the wait for the prefill -- and the two parts
-        # one after the other, for comparison with the concurrent step.
-        Kc = min(K, 200)
+
+    # ---- device-timed region: K steps back to back, nothing between them.
+    t_start, t_end = ev(), ev()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    h0 = time.time()
+    t_start.record(stream)
+    for _ in range(K):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    h1 = time.time()
+    dist_barrier(world)
+    clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    flags = pa.pa_get_error(err, stream)
+    if flags:
+        raise RuntimeError(f"device error flags {flags} in the timed region")
+    max_ms = dist_max(total_ms, world)
+    ms_per_step = max_ms / K
+    total_s = max_ms / 1e3
+    value = step_b * K * world / total_s / 1e9
+    seq_steps = S * K * world / total_s
+
+    # ---- kernel timings for the roofline, after the timed region.
+    seq_ms = pre_t = None
+    if mixed is None:
+        # pa_decode alone (planning + decode kernels), back to back: the K/V
+        # it reads per call (>= 1.4 GB on the full-size batches) is far larger than L2.
+        dec_t = time_calls(decode, stream, dev, max(K, 100), 50)
+        dec_ms = dec_t["mean_ms_back_to_back"]
+    else:
+        # Component pass: scatter, decode, prefill one after the other with
+        # events around the two attention calls -- inside the concurrent step
+        # the decode's events would also span the prefill; the decode between
+        # two prefills also flushes the prefill's 105 MB of K/V from L2.
+        Kc = max(K, 50)
         dec_s, dec_e = [ev() for _ in range(Kc)], [ev() for _ in range(Kc)]
         pre_s, pre_e = [ev() for _ in range(Kc)], [ev() for _ in range(Kc)]
         c0_, c1_ = ev(), ev()
@@ -484,50 +674,62 @@ def run_ours(args, rank, world, local):
             pre_e[i].record(stream)
         c1_.record(stream)
         torch.cuda.synchronize(dev)
-        dec_ms = [a.elapsed_time(b) for a, b in zip(dec_s, dec_e)]
-        pre_ms = [a.elapsed_time(b) for a, b in zip(pre_s, pre_e)]
+        dec_t = call_stats([a.elapsed_time(b) for a, b in zip(dec_s, dec_e)])
+        pre_t = call_stats([a.elapsed_time(b) for a, b in zip(pre_s, pre_e)])
         seq_ms = c0_.elapsed_time(c1_) / Kc
+        dec_ms = dec_t["mean_ms"]
+    if pa.pa_get_error(err, stream):
+        raise RuntimeError("device error flags in the kernel-timing pass")
 
-    # ---- device-timed region.  The decode call is bracketed by its own events
-    # on every 16th step only: an event recorded between two kernels stops the
-    # next one from starting early behind the previous one (programmatic
-    # dependent launch), which a user's back-to-back steps do not pay.
-    sampled = list(range(0, K, 16))
-    if mixed is None:
-        dec_s, dec_e = {i: ev() for i in sampled}, {i: ev() for i in sampled}
-    t_start, t_end = ev(), ev()
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    dist_barrier(world)
-    torch.cuda.synchronize(dev)
-    h0 = time.time()
-    t_start.record(stream)
-    for i in range(K):
-        pa.pa_reshape_and_cache(k_new, v_new, w.k_pool, w.v_pool, slots_d, err, stream)
-        if mixed is not None:
-            mixed_step()
-        elif i in dec_s:
-            dec_s[i].record(stream)
-            decode()
-            dec_e[i].record(stream)
-        else:
-            decode()
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    h1 = time.time()
-    dist_barrier(world)
-    clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if mixed is None:
-        dec_ms = [dec_s[i].elapsed_time(dec_e[i]) for i in sampled]
-    flags = pa.pa_get_error(err, stream)
-    if flags:
-        raise RuntimeError(f"device error flags {flags} in the timed region")
-    max_ms = dist_max(total_ms, world)
-    total_s = max_ms / 1e3
-    value = step_b * K * world / total_s / 1e9
-    seq_steps = S * K * world / total_s
+    peak, peak_kind = load_peaks()
+    dec_note = None
+    if dec_ms > ms_per_step:
+        # the decode call cannot take longer than the step that contains it
+        dec_note = (f"decode call timed at {dec_ms:.4f} ms, longer than the step ({ms_per_step:.4f} ms): the "
+                    "roofline uses the step time")
+        dec_ms = ms_per_step
+    achieved = dbytes / (dec_ms / 1e3) / 1e9
+    sha = kernel_sha()
+    traffic = (TRAFFIC["bytes_per_launch"] if name == "llama13b" and TRAFFIC["kernel_sha256_prefix"] == sha
+               else None)
+    launches = 3 + (1 if mixed is not None else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": workload_config(name, w),
+        "parallelism": f"replicas x{world}",
+        "seq_steps_per_s": seq_steps,
+        "hbm_frac_of_measured_peak": value / world / peak,
+        "hbm_frac_of_nominal_8tbs": value / world / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "kernel": "pa_decode call (planning kernel + persistent decode kernel)",
+                     "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": dec_ms,
+                     "calls": dec_t, "kernel_sha256_prefix": sha},
+        "gpu_launches": launches * K,
+        "clocks": clocks.summary(h0, h1),
+    }
+    if dec_note:
+        line["roofline"]["note"] = dec_note
+    if "unique_kv_bytes" in w.extra:
+        line["config"]["unique_kv_bytes"] = w.extra["unique_kv_bytes"]
+        line["roofline"]["note"] = ("logical bytes: shared prompt blocks are counted once per sample that reads "
+                                    "them; the unique K/V footprint is config.unique_kv_bytes")
+    if mixed is not None:
+        line["roofline"]["note"] = ("decode kernel timed alone in a component pass after the timed region (inside "
+                                    "the concurrent step its events would also span the prefill)")
+        line["sequential_ms_per_step"] = seq_ms
+        line["concurrent_speedup_vs_sequential"] = seq_ms / ms_per_step
+        bf16_peak = load_tensor_peak()
+        pre_avg_s = pre_t["mean_ms"] / 1e3
+        line["prefill"] = {"bound": "tensor", "achieved": pflops / pre_avg_s / 1e12, "unit": "TFLOP/s",
+                           "peak": bf16_peak[0], "frac": pflops / pre_avg_s / 1e12 / bf16_peak[0],
+                           "peak_kind": bf16_peak[1], "algorithmic_flops_per_launch": pflops,
+                           "avg_launch_ms": pre_t["mean_ms"], "calls": pre_t,
+                           "kernel_sha256_prefix": kernel_sha(("pa_prefill.cu", "pa_common.cuh"))}
+    if secondary:
+        return line
 
     # ---- end to end through the API: pinned host inputs in, result out, every step.
     # The copies run on their own streams with two sets of device buffers, so
@@ -594,87 +796,80 @@ def run_ours(args, rank, world, local):
     e2e_value = step_b * Ke * world / (e2e_ms / 1e3) / 1e9
     if not torch.equal(host_out[0].view(torch.int16), out.cpu().view(torch.int16)):
         raise RuntimeError("the end-to-end result differs from the device-timed step's")
-
-    peak, peak_kind = load_peaks()
-    dec_avg_s = statistics.mean(dec_ms) / 1e3
-    achieved = dbytes / dec_avg_s / 1e9
-    sha = kernel_sha()
-    traffic = (TRAFFIC["bytes_per_launch"] if name == "llama13b" and TRAFFIC["kernel_sha256_prefix"] == sha
-               else None)
-    launches = 3 + (1 if mixed is not None else 0)
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic",
-        "config": {**workload_config(name, w), "parallelism": f"replicas x{world}"},
-        "seq_steps_per_s": seq_steps,
-        "hbm_frac_of_measured_peak": value / world / peak,
-        "hbm_frac_of_nominal_8tbs": value / world / 8000.0,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": "pa_decode call (planning kernel + persistent decode kernel)",
-                     "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": dec_avg_s * 1e3,
-                     "timed_calls": len(dec_ms),
-                     "kernel_sha256_prefix": sha},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / Ke, "steps": Ke,
-                "overlap": "copies on their own streams, double-buffered, overlapping the previous step"},
-        "gpu_launches": launches * K,
-        "clocks": clocks.summary(h0, h1),
-    }
-    if "unique_kv_bytes" in w.extra:
-        line["config"]["unique_kv_bytes"] = w.extra["unique_kv_bytes"]
-        line["roofline"]["note"] = ("logical bytes: shared prompt blocks are counted once per sample that reads "
-                                    "them; the unique K/V footprint is config.unique_kv_bytes")
-    if mixed is not None:
-        line["roofline"]["note"] = ("decode kernel timed alone in a component pass before the timed region (inside "
-                                    "the concurrent step its events would also span the prefill)")
-        line["sequential_ms_per_step"] = seq_ms
-        line["concurrent_speedup_vs_sequential"] = seq_ms / (max_ms / K)
-        bf16_peak = load_tensor_peak()
-        pre_avg_s = statistics.mean(pre_ms) / 1e3
-        line["prefill"] = {"bound": "tensor", "achieved": pflops / pre_avg_s / 1e12, "unit": "TFLOP/s",
-                           "peak": bf16_peak[0], "frac": pflops / pre_avg_s / 1e12 / bf16_peak[0],
-                           "peak_kind": bf16_peak[1], "algorithmic_flops_per_launch": pflops,
-                           "avg_launch_ms": pre_avg_s * 1e3,
-                           "tensor_flops_executed_per_launch": pflops * 3 // 2}
+    line["e2e"] = {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "ms_per_step": e2e_ms / Ke, "steps": Ke,
+                   "overlap": "copies on their own streams, double-buffered, overlapping the previous step"}
     if name == "tiny":
         line["graph_replay"] = graph_replay_comparison(pa, w, dev, stream)
     if rank == 0 and not args.no_cpu_baseline:
-        import oracle
-
-        host = {k: getattr(w, k).cpu() for k in ("k_pool", "v_pool", "q", "k_new", "v_new")}
-        t_rep, reps = OracleStep(w, host).time(args.cpu_budget)
-        thr = oracle.num_threads()
-        line["cpu_baseline"] = {"value": (dbytes + scatter_bytes(S, H, D, elt)) / t_rep / 1e9, "unit": "GB/s",
-                                "cores": thr, "kind": "oracle",
-                                "sample": f"decode part of the step (scatter + decode), {reps} repetitions, "
-                                          f"{t_rep * reps:.1f} s wall"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+        line["cpu_baseline"] = cpu_baseline_decode(w, args.cpu_budget, elt)
+    return line
 
 
-def run_prefill(args, rank, world, local):
-    """One prefill step = four 2048-token prompts' K/V scattered into their
-    pages, then one pa_prefill_chunk over the four prompts (context 0).  value: algorithmic
-    TFLOP/s of the step; roofline: the prefill kernel alone (per-call events
-    on every 16th step), against the measured dense tensor peak (fp16 and
-    bf16 run at the same rate); e2e: pinned host inputs in and the output
-    out every step, copies pipelined; cpu_baseline: the oracle on four
-    16-row sub-chunks spread over the first prompt (a sub-chunk starting at
-    row a has context a, so its rows are exactly those rows of the prompt)."""
-    import numpy as np
+# Configurations the default run also times after the headline (same
+# --steps / --warmup), each nested under "other_configs" in the same line.
+OTHER_CONFIGS = ("tiny", "shared_prefix", "long_context", "mixed", "budget512", "prefill", "swap")
+
+
+def secondary_summary(line: dict) -> dict:
+    keep = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "roofline", "clocks",
+            "seq_steps_per_s", "prefill", "sequential_ms_per_step", "concurrent_speedup_vs_sequential",
+            "gpu_launches", "copy_blocks_roofline", "sweep_by_block_size")
+    return {k: line[k] for k in keep if k in line}
+
+
+def run_ours(args, rank, world, local):
     import torch
 
     import __graft_entry__
 
     __graft_entry__.build()
+    line = measure_decode(args, rank, world, local, args.workload)
+    if args.workload == "llama13b" and not args.no_other_configs:
+        others = {}
+        for name in OTHER_CONFIGS:
+            torch.cuda.empty_cache()
+            if name == "prefill":
+                sub = measure_prefill(args, rank, world, local, name, secondary=True)
+            elif name == "swap":
+                sub = measure_swap(args, rank, world, local)
+            else:
+                sub = measure_decode(args, rank, world, local, name, secondary=True)
+            others[name] = secondary_summary(sub)
+        line["other_configs"] = others
+        line["gpu_launches_other_configs"] = sum(o["gpu_launches"] for o in others.values())
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_prefill(args, rank, world, local):
+    import __graft_entry__
+
+    __graft_entry__.build()
+    line = measure_prefill(args, rank, world, local, args.workload)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_prefill(args, rank, world, local, name, secondary=False):
+    """One prefill step = four 2048-token prompts' K/V scattered into their
+    pages, then one pa_prefill_chunk over the four prompts (context 0).  value: algorithmic
+    TFLOP/s of the step; roofline: the prefill kernel alone (calls back to
+    back after the timed region; K/V and queries, 252 MB, exceed L2), against
+    the measured dense tensor peak (fp16 and bf16 run at the same rate); e2e:
+    pinned host inputs in and the output out every step, copies pipelined;
+    cpu_baseline: the oracle on four 16-row sub-chunks spread over the first
+    prompt (a sub-chunk starting at row a has context a, so its rows are
+    exactly those rows of the prompt).  `secondary` skips the end-to-end pass
+    and the CPU baseline.  Returns the JSON line as a dict."""
+    import numpy as np
+    import torch
+
     import paged_kv_cache_35_gb300 as pa
     import pa_workloads as W
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    name = args.workload
     dtype = "f16" if name == "prefill_f16" else "bf16"
     NP, L = 4, 2048  # prompts, tokens per prompt
     T = NP * L
@@ -710,8 +905,6 @@ def run_prefill(args, rank, world, local):
 
     K = args.steps
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    sampled = list(range(0, K, 16))
-    p_s, p_e = {i: ev() for i in sampled}, {i: ev() for i in sampled}
     t_start, t_end = ev(), ev()
     clocks = ClockSampler(local)
     clocks.start()
@@ -720,14 +913,8 @@ def run_prefill(args, rank, world, local):
     torch.cuda.synchronize(dev)
     h0 = time.time()
     t_start.record(stream)
-    for i in range(K):
-        pa.pa_reshape_and_cache(m.chunk_k, m.chunk_v, w.k_pool, w.v_pool, slots_d, err, stream)
-        if i in p_s:
-            p_s[i].record(stream)
-            prefill()
-            p_e[i].record(stream)
-        else:
-            prefill()
+    for _ in range(K):
+        step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     h1 = time.time()
@@ -737,8 +924,44 @@ def run_prefill(args, rank, world, local):
     if flags:
         raise RuntimeError(f"device error flags {flags} in the timed region")
     max_ms = dist_max(t_start.elapsed_time(t_end), world)
+    ms_per_step = max_ms / K
     value = flops * K * world / (max_ms / 1e3) / 1e12
-    pre_ms = [p_s[i].elapsed_time(p_e[i]) for i in sampled]
+    pre_t = time_calls(prefill, stream, dev, max(K, 100), 50)
+    pre_ms = pre_t["mean_ms_back_to_back"]
+    pre_note = None
+    if pre_ms > ms_per_step:
+        pre_note = (f"prefill call timed at {pre_ms:.4f} ms, longer than the step ({ms_per_step:.4f} ms): the "
+                    "roofline uses the step time")
+        pre_ms = ms_per_step
+    if pa.pa_get_error(err, stream):
+        raise RuntimeError("device error flags in the kernel-timing pass")
+    peak, peak_kind = load_tensor_peak()
+    pf_sha = kernel_sha(("pa_prefill.cu", "pa_common.cuh"))
+    pf_traffic = (PREFILL_TRAFFIC[dtype]["bytes_per_launch"] if PREFILL_TRAFFIC["kernel_sha256_prefix"] == pf_sha
+                  else None)
+    achieved = flops / (pre_ms / 1e3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[name], "prompts": NP, "tokens_per_prompt": L, "context_before": 0,
+                   "num_heads": H, "head_dim": D, "block_size": B, "kv_dtype": dtype,
+                   "l2": "no flush: inputs larger than L2 (per step the scatter reads 168 MB of new K/V and "
+                         "writes it to the pool, the prefill reads it and 84 MB of queries and writes 84 MB)"},
+        "parallelism": f"replicas x{world}",
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": pf_traffic, "peak_kind": peak_kind,
+                     "kernel": "prefill_kernel (pa_prefill_chunk)", "algorithmic_flops_per_launch": flops,
+                     "avg_launch_ms": pre_ms, "calls": pre_t,
+                     "kernel_sha256_prefix": pf_sha,
+                     "traffic_source": "ncu DRAM bytes (read + write) of one launch of this workload"},
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(h0, h1),
+    }
+    if pre_note:
+        line["roofline"]["note"] = pre_note
+    if secondary:
+        return line
 
     # ---- end to end: pinned host inputs (q, the prompt's K/V, slots, table,
     # offsets) in and the output out every step, double-buffered on their own streams
@@ -795,34 +1018,9 @@ def run_prefill(args, rank, world, local):
     if pa.pa_get_error(err, stream):
         raise RuntimeError("device error flags in the end-to-end pass")
 
-    peak, peak_kind = load_tensor_peak()
-    pf_sha = kernel_sha(("pa_prefill.cu", "pa_common.cuh"))
-    pf_traffic = (PREFILL_TRAFFIC[dtype]["bytes_per_launch"] if PREFILL_TRAFFIC["kernel_sha256_prefix"] == pf_sha
-                  else None)
-    pre_avg_s = statistics.mean(pre_ms) / 1e3
-    achieved = flops / pre_avg_s / 1e12
-    line = {
-        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[name], "prompts": NP, "tokens_per_prompt": L, "context_before": 0,
-                   "num_heads": H, "head_dim": D, "block_size": B, "kv_dtype": dtype,
-                   "l2": "no flush: inputs larger than L2 (per step the scatter reads 168 MB of new K/V and "
-                         "writes it to the pool, the prefill reads it and 84 MB of queries and writes 84 MB)",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": pf_traffic, "peak_kind": peak_kind,
-                     "kernel": "prefill_kernel (pa_prefill_chunk)", "algorithmic_flops_per_launch": flops,
-                     "avg_launch_ms": pre_avg_s * 1e3, "timed_calls": len(pre_ms),
-                     "tensor_flops_executed_per_launch": flops * (3 if dtype == "bf16" else 2) // 2,
-                     "kernel_sha256_prefix": pf_sha, "traffic_source": PREFILL_TRAFFIC[dtype]["source"],
-                     "note": "bf16: P V runs as two products (P_hi, P_lo); fp16: one"},
-        "e2e": {"value": flops * Ke * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / Ke, "steps": Ke,
-                "overlap": "copies on their own streams, double-buffered, overlapping the previous step"},
-        "gpu_launches": 2 * K,
-        "clocks": clocks.summary(h0, h1),
-    }
+    line["e2e"] = {"value": flops * Ke * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / Ke, "steps": Ke,
+                   "overlap": "copies on their own streams, double-buffered, overlapping the previous step"}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
 
@@ -846,8 +1044,7 @@ def run_prefill(args, rank, world, local):
                                 "cores": oracle.num_threads(), "kind": "oracle",
                                 "sample": f"{len(starts)} x {n} query rows (contexts 1..{starts[-1] + n}), "
                                           f"{reps} repetitions, {el:.1f} s wall"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 def graph_replay_comparison(pa, w, dev, stream, n=2000):
@@ -903,12 +1100,22 @@ def graph_replay_comparison(pa, w, dev, stream, n=2000):
 
 
 def run_swap(args, rank, world, local):
+    line = measure_swap(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_swap(args, rank, world, local):
     """Block swap between the GPU pool and a pinned host pool, by block size:
     the swap side of the pages' swap-versus-recompute comparison.  Each
     replica swaps the K/V of 8 requests x 2048 tokens (40 heads x 128, fp16)
     out to the host pool and back in, through pa_swap_blocks with the blocks
     scattered over a pool twice that size; the link's ceiling is one
-    contiguous copy of the same bytes, timed the same way in the same run."""
+    contiguous copy of the same bytes, timed the same way in the same run.
+    The same blocks are also copied inside the GPU pool with pa_copy_blocks
+    (the copy-on-write copy at batch scale: scattered sources to scattered
+    destinations), against a contiguous device copy of the same bytes and
+    the measured copy peak.  Returns the JSON line as a dict."""
     import numpy as np
     import torch
 
@@ -937,6 +1144,9 @@ def run_swap(args, rank, world, local):
 
     sweep = []
     err = pa.new_error_flag(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    h0 = time.time()
     for B in (16, 32, 64, 128, 256):
         nb = tokens // B
         gk = W.normal((2 * nb, H, B, D), 71, torch.float16, dev)
@@ -953,13 +1163,23 @@ def run_swap(args, rank, world, local):
         slab_k, slab_v = gk[:nb], gv[:nb]
         t_cout = timed(lambda: (ck.copy_(slab_k, non_blocking=True), cv.copy_(slab_v, non_blocking=True)))
         t_cin = timed(lambda: (slab_k.copy_(ck, non_blocking=True), slab_v.copy_(cv, non_blocking=True)))
+        # copy-on-write copies at batch scale: nb scattered sources to nb other scattered blocks
+        perm = torch.randperm(2 * nb, generator=g)
+        copy_pairs = torch.stack([perm[:nb], perm[nb:]], 1).to(torch.int32).to(dev)
+        t_copy = timed(lambda: pa.pa_copy_blocks(gk, gv, copy_pairs, err, stream))
+        dst_k, dst_v = gk[nb:], gv[nb:]
+        t_dcopy = timed(lambda: (dst_k.copy_(slab_k), dst_v.copy_(slab_v)))
         if pa.pa_get_error(err, stream):
             raise RuntimeError("device error flags during the swap sweep")
         sweep.append({"block_size": B, "blocks": nb, "bytes": nbytes,
                       "swap_out_ms": t_out, "swap_in_ms": t_in,
                       "swap_out_GBs": nbytes / t_out / 1e6, "swap_in_GBs": nbytes / t_in / 1e6,
-                      "contiguous_out_GBs": nbytes / t_cout / 1e6, "contiguous_in_GBs": nbytes / t_cin / 1e6})
+                      "contiguous_out_GBs": nbytes / t_cout / 1e6, "contiguous_in_GBs": nbytes / t_cin / 1e6,
+                      "copy_blocks_ms": t_copy, "copy_blocks_GBs": 2 * nbytes / t_copy / 1e6,
+                      "contiguous_device_copy_GBs": 2 * nbytes / t_dcopy / 1e6})
         del gk, gv, ck, cv
+    h1 = time.time()
+    clocks.stop()
     head = sweep[0]
     value = 2 * head["bytes"] * world / ((head["swap_out_ms"] + head["swap_in_ms"]) / 1e3) / 1e9
     link = 2 * head["bytes"] / ((head["bytes"] / head["contiguous_out_GBs"] + head["bytes"] / head["contiguous_in_GBs"])
@@ -972,9 +1192,18 @@ def run_swap(args, rank, world, local):
             "roofline": {"bound": "link", "achieved": value / world, "peak": link, "unit": "GB/s",
                          "frac": value / world / link, "traffic": None,
                          "peak_kind": "measured in this run: one contiguous copy of the same bytes each way"},
-            "gpu_launches": 2 * K, "sweep_by_block_size": sweep}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+            "gpu_launches": 2 * K, "sweep_by_block_size": sweep,
+            "clocks": clocks.summary(h0, h1)}
+    peak, peak_kind = load_peaks()
+    cb = head["copy_blocks_GBs"]
+    line["copy_blocks_roofline"] = {
+        "bound": "hbm", "achieved": cb, "peak": peak, "unit": "GB/s", "frac": cb / peak, "traffic": None,
+        "peak_kind": f"{peak_kind} copy bandwidth", "kernel": "copy_blocks_kernel (pa_copy_blocks)",
+        "algorithmic_bytes_per_launch": 2 * head["bytes"], "avg_launch_ms": head["copy_blocks_ms"],
+        "note": f"{head['blocks']} pairs of 16-token blocks (40 heads x 128, fp16), K and V read and written; "
+                "the contiguous device copy of the same bytes in this run reached "
+                f"{head['contiguous_device_copy_GBs']:.0f} GB/s"}
+    return line
 
 
 def run_prefix_cache(args, rank, world, local):
@@ -1181,6 +1410,11 @@ def main():
                     help="llama13b (the headline configuration) or another configuration")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU-oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="long_context only: the first N sequences of the same length draw (a smaller case for "
+                         "profiling captures); 0 = all 256")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="default run: time only the headline configuration")
     args = ap.parse_args()
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

@@ -62,12 +62,19 @@ def lib():
         L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
         L.oracle_bf16_to_double.restype = ctypes.c_double
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_set_num_threads.argtypes = [i]
+        L.oracle_set_num_threads.restype = ctypes.c_int
         _lib = L
     return _lib
 
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads of the oracle's OpenMP loops from now on; returns the count in effect."""
+    return int(lib().oracle_set_num_threads(int(n)))
 
 
 def _bits(t) -> np.ndarray:

@@ -84,6 +84,19 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads the parallel loops use from now on (n >= 1); returns the number in
+ * effect afterwards (1 without OpenMP).  Only the CPU-baseline timing uses
+ * it, to time the oracle single-threaded beside its OpenMP run. */
+int oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
+
 /*
  * Attention of one query row over the first n tokens of one sequence's
  * paged K/V for one head.  Steps, in the order the definition gives them:
@@ -269,10 +282,6 @@ int oracle_reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new, uint1
   return OR_OK;
 }
 
-/*
- * Copy-on-write block copy: for each pair (src, dst) in order, every slot of
- * every head of block src is copied bitwise into block dst, in K and in V.
- */
 /* Block swap between two pools ([summary] section 5: a preempted sequence's
  * KV blocks are swapped out to CPU memory and back in; [cb] "오프로딩": the
  * blocks are copied into a pinned CPU buffer and copied back on resume).
@@ -296,6 +305,10 @@ int oracle_swap_blocks(const uint16_t* src_k, const uint16_t* src_v, int src_num
   return skipped;
 }
 
+/*
+ * Copy-on-write block copy: for each pair (src, dst) in order, every slot of
+ * every head of block src is copied bitwise into block dst, in K and in V.
+ */
 int oracle_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32_t* pairs, int num_pairs,
                        int num_heads, int head_dim, int block_size, int num_blocks) {
   const int64_t per_block = (int64_t)num_heads * block_size * head_dim;

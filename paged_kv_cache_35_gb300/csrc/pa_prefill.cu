@@ -126,11 +126,11 @@ struct PfSlot {
 struct PfBars {
   uint64_t item_full[kItemSlots];  // the loader wrote the slot, one phase per use
   uint64_t q_full, q_empty;  // query tile loaded / its last S = Q K^T done
-  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t k_full[kKStages];  // (a K stage is free again when its S = Q K^T is done: s_full)
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2];      // per score buffer
+  uint64_t s_full[2];      // per score buffer; also frees K stage x % 2 (kKStages == 2)
   uint64_t p_full[2][2];   // [half][buffer]: every row wrote P_h(j), buffer j % 2, one phase per use
-  uint64_t pv_done[2][2];  // per half: P_h(j) V complete, barrier j % 2, one phase per use
+  uint64_t pv_done[2];     // both halves' P(j) V complete, barrier j % 2, one phase per use
   uint64_t v_zeroed;       // V rows past the context zeroed (last key tile)
   uint64_t xbar[4];        // per lane quarter: both halves' (max, sum) written (end of an item)
   uint64_t o_free;         // every softmax warp has read the output accumulators (end of an item)
@@ -144,6 +144,7 @@ struct PfBars {
 };
 constexpr uint32_t kPfSmemBytes = kOffBar + sizeof(PfBars) + 1024;  // + alignment slack
 static_assert(kPfSmemBytes <= 227 * 1024, "shared memory beyond the per-CTA limit");
+static_assert(kKStages == 2, "s_full[x & 1] frees K stage x % kKStages");
 
 struct PrefillArgs {
   void* out;
@@ -464,7 +465,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(&bars.q_empty, 1);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bars.k_full[i], 1);
-      mbar_init(&bars.k_empty[i], 1);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bars.v_full[i], 1);
@@ -472,11 +472,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     mbar_init(&bars.s_full[0], 1);
     mbar_init(&bars.s_full[1], 1);
+    mbar_init(&bars.pv_done[0], 1);
+    mbar_init(&bars.pv_done[1], 1);
     for (int hh = 0; hh < 2; ++hh) {
       mbar_init(&bars.p_full[hh][0], 4);
       mbar_init(&bars.p_full[hh][1], 4);
-      mbar_init(&bars.pv_done[hh][0], 1);
-      mbar_init(&bars.pv_done[hh][1], 1);
     }
     mbar_init(&bars.v_zeroed, 4);
     mbar_init(&bars.o_free, 8);
@@ -576,7 +576,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (t < it.n_kv) {  // K of tile t
           const int x = g + t;
           const int stg = x % kKStages;
-          if (lane == 0) wk = mbar_wait(&bars.k_empty[stg], ((x / kKStages) & 1) ^ 1, abort_flag, a.err_flag);
+          // stage x % 2 held K(x-2): free once S(x-2) is done, the previous phase of s_full[x & 1]
+          if (lane == 0) wk = mbar_wait(&bars.s_full[stg], ((x / kKStages) & 1) ^ 1, abort_flag, a.err_flag);
           if (!__shfl_sync(0xffffffffu, wk, 0)) {
             ok = false;
             break;
@@ -651,8 +652,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint32_t koff = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
             umma_f16(d, qdesc + koff, kdesc + koff, a.idesc_s, kk > 0);
           }
-          umma_commit(&bars.s_full[x & 1]);
-          umma_commit(&bars.k_empty[x % kKStages]);
+          umma_commit(&bars.s_full[x & 1]);  // the scores, and K stage x % 2 free again
           if (t == n_kv - 1) umma_commit(&bars.q_empty);
           return true;
         };
@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                             vdesc + (((hh * 4 + kk) * 2048) >> 4), a.idesc_pv, (kk > 0 || part > 0) ? 1u : first);
               }
             }
-            umma_commit(&bars.pv_done[hh][x & 1]);
+            if (hh == 1) umma_commit(&bars.pv_done[x & 1]);  // both halves' products (issued in order)
           }
           if (!ok) break;
           umma_commit(&bars.v_empty[x % kVStages]);
@@ -819,7 +819,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // A rescale of O_h also needs P_h(x-1) V (same item) in it.
         const bool any_resc = t > 0 && __any_sync(0xffffffffu, resc);
         if (any_resc)
-          ok = mbar_wait(&bars.pv_done[half][(x - 1) & 1], ((x - 1) >> 1) & 1, abort_flag, a.err_flag);
+          ok = mbar_wait(&bars.pv_done[(x - 1) & 1], ((x - 1) >> 1) & 1, abort_flag, a.err_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -872,7 +872,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!ok) break;
       // ---- epilogue: merge the two half-rows (log-sum-exp), write this half's 64 output columns
       const int xl_ = g + n_kv - 1;  // the item's last key tile
-      ok = mbar_wait(&bars.pv_done[half][xl_ & 1], (xl_ >> 1) & 1, abort_flag, a.err_flag);
+      ok = mbar_wait(&bars.pv_done[xl_ & 1], (xl_ >> 1) & 1, abort_flag, a.err_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       bars.xm[half][r] = m_used;
@@ -881,7 +881,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (lane == 0) mbar_arrive(&bars.xbar[quarter]);
       ok = mbar_wait(&bars.xbar[quarter], k & 1, abort_flag, a.err_flag);
       // the partner's output must be complete too before its columns are read
-      if (ok) ok = mbar_wait(&bars.pv_done[1 - half][xl_ & 1], (xl_ >> 1) & 1, abort_flag, a.err_flag);
+      // (pv_done covers the partner half's product of the last tile too)
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;

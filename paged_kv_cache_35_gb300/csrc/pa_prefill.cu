@@ -161,6 +161,7 @@ struct PrefillArgs {
   int pool_rows;      // num_blocks * H * B: any row at or past it reads zeros
   int num_chunks;
   int qtiles;         // query tiles per chunk in the grid: ceil(max_q_len / 128)
+  int head_group;     // heads dealt together (num_heads: one group)
   float qscale;       // scale * log2(e)
   uint32_t idesc_s;   // instruction descriptors
   uint32_t idesc_pv;
@@ -370,13 +371,24 @@ struct PfItem {
 
 enum { kItemRun = 0, kItemEmpty = 1, kItemBadLength = 2 };
 
-// Item at position `pos` of the longest-first list.  The list is (chunk,
-// query tile) pairs in `order` (or, past kPfRankMax pairs, later query tiles
-// first), each expanded over the heads.
+// Item at position `pos` of the list.  The heads are dealt in groups of
+// a.head_group: within a group the list is the (chunk, query tile) pairs in
+// `order` (or, past kPfRankMax pairs, later query tiles first), each expanded
+// over the group's heads, so that while a group runs, the CTAs read the K/V of
+// its heads only.  Odd groups take the pairs in reverse (shortest first), so
+// that the rounds dealt forward and backward over the CTAs stay balanced
+// across group boundaries; one group (every head) is plain longest-first.
 __device__ __forceinline__ int pf_item(const PrefillArgs& a, const uint16_t* order, int npairs, int pos, PfItem& it) {
   const int H = a.num_heads;
-  const int rank = pos / H;
-  it.h = pos - rank * H;
+  const int G = a.head_group;
+  const int per_group = npairs * G;  // positions of a full group (fits int: the host bounds npairs * H)
+  const int gi = pos / per_group;
+  const int within = pos - gi * per_group;
+  const int h0 = gi * G;
+  const int gsz = min(G, H - h0);  // the last group may hold fewer heads
+  int rank = within / gsz;
+  it.h = h0 + within - rank * gsz;
+  if (gi & 1) rank = npairs - 1 - rank;
   int c, qt;
   if (npairs <= kPfRankMax) {
     const int pair = order[rank];
@@ -1133,6 +1145,18 @@ int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_
   // persistent: at most one CTA per SM (shared and tensor memory allow one)
   long long ctas = max_ctas > 0 && max_ctas < sms ? max_ctas : sms;
   if (ctas > n_items) ctas = n_items;
+  // A launch of many rounds deals its heads in groups of at least three
+  // rounds' worth of items, so that the CTAs stream one group's K/V at a time
+  // (it can stay in L2 for the group's other query tiles) instead of every head's.
+  a.head_group = num_heads;
+  if (n_items >= 8 * ctas) {
+    const long long npairs = (long long)a.qtiles * num_chunks;
+    const long long g = (3 * ctas + npairs - 1) / npairs;
+    if (g < num_heads) {
+      const int ngroups = num_heads / (int)g;
+      a.head_group = (num_heads + ngroups - 1) / ngroups;
+    }
+  }
   kern<<<dim3((unsigned)ctas), pa::kPfThreads, pa::kPfSmemBytes, (cudaStream_t)stream>>>(tm_q, tm_k, tm_v, a);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

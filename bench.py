@@ -51,8 +51,8 @@ TRAFFIC = {"bytes_per_launch": 1488338856, "kernel_sha256_prefix": "a53b700b600e
 # DRAM bytes (read + write) per pa_prefill_chunk call on the four-prompt
 # prefill workloads, from ncu captures of one launch each; valid only for the
 # prefill kernel source whose sha256 prefix is given.
-PREFILL_TRAFFIC = {"kernel_sha256_prefix": "8984a9047cd62c1a",
-                   "bf16": {"bytes_per_launch": 1222296720}, "f16": {"bytes_per_launch": 1179484712}}
+PREFILL_TRAFFIC = {"kernel_sha256_prefix": "ea05c77b06d2bae9",
+                   "bf16": {"bytes_per_launch": 342607360}, "f16": {"bytes_per_launch": 342570752}}
 
 
 def kernel_sha(files=("pa_decode.cu", "pa_common.cuh")) -> str:

@@ -305,3 +305,15 @@ def test_prefill_long_chunk(pa, B):
     ref, kb, vb = oracle_prefill(m)
     assert np.array_equal(oracle.pool_bits(kp.cpu()), kb) and np.array_equal(oracle.pool_bits(vp.cpu()), vb)
     assert_attn_close(out, ref, "f32", f"prefill 2048-query chunk, block {B}")
+
+
+def test_prefill_head_groups(pa):
+    """A launch of at least eight rounds of the grid deals its heads in groups
+    (here 4 chunks x 4 query tiles x 80 heads = 1280 items: two groups of 40
+    heads, the second taking its query tiles shortest first).  The order is
+    only a schedule: every row must match the oracle."""
+    m = W.small_prefill(chunk_lens=(512, 512, 512, 512), ctx_before=(0, 50, 130, 300), H=80, B=16)
+    out, flags, _, _ = run_prefill(pa, m, "f32")
+    assert flags == 0
+    ref, _, _ = oracle_prefill(m)
+    assert_attn_close(out, ref, "f32", "prefill with head groups")

@@ -45,14 +45,14 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, from an ncu capture of one launch (dram__bytes_read.sum +
 # dram__bytes_write.sum); valid only for the decode kernel source whose
 # sha256 prefix is given (otherwise reported as null).
-TRAFFIC = {"bytes_per_launch": 1488338856, "kernel_sha256_prefix": "a53b700b600e6a63"}
+TRAFFIC = {"bytes_per_launch": 1488302592, "kernel_sha256_prefix": "71fdb188290db9f5"}
 
 
 # DRAM bytes (read + write) per pa_prefill_chunk call on the four-prompt
 # prefill workloads, from ncu captures of one launch each; valid only for the
 # prefill kernel source whose sha256 prefix is given.
-PREFILL_TRAFFIC = {"kernel_sha256_prefix": "ea05c77b06d2bae9",
-                   "bf16": {"bytes_per_launch": 342607360}, "f16": {"bytes_per_launch": 342570752}}
+PREFILL_TRAFFIC = {"kernel_sha256_prefix": "4962eb099e81b390",
+                   "bf16": {"bytes_per_launch": 341745664}, "f16": {"bytes_per_launch": 341157120}}
 
 
 def kernel_sha(files=("pa_decode.cu", "pa_common.cuh")) -> str:

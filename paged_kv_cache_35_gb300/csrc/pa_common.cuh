@@ -204,6 +204,7 @@ int prefill_check(void* out, int out_dtype, const void* q, const int32_t* cu_q_l
 int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_before,
                    const void* k_pool, const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
                    int num_chunks, int total_q, int max_q_len, int num_heads, int head_dim, int block_size,
-                   int num_blocks, float scale, int dtype, int32_t* err_flag, int max_ctas, void* stream);
+                   int num_blocks, float scale, int dtype, int32_t* err_flag, int max_ctas, int head_group,
+                   void* stream);
 
 }  // namespace pa_host

@@ -886,12 +886,13 @@ int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int
   if (sms <= 0) return PA_ERR_CUDA;
   int cap = prefill_sms > 0 ? (prefill_sms < sms ? prefill_sms : sms) : (sms * PA_MIXED_PREFILL_SHARE + 50) / 100;
   if (cap < 1) cap = 1;
-  auto prefill = [&](int ctas) {
+  auto prefill = [&](int ctas, int head_group) {
     return pa_host::prefill_launch(pf_out, pf_out_dtype, pf_q, cu_q_lens, ctx_before, k_pool, v_pool,
                                    pf_block_tables, pf_max_blocks_per_seq, num_chunks, total_q, max_q_len,
-                                   num_heads, head_dim, block_size, num_blocks, scale, dtype, err_flag, ctas, stream);
+                                   num_heads, head_dim, block_size, num_blocks, scale, dtype, err_flag, ctas,
+                                   head_group, stream);
   };
-  if (dec_empty) return pf_empty ? PA_OK : prefill(0);
+  if (dec_empty) return pf_empty ? PA_OK : prefill(0, 0);
   cudaStream_t s = (cudaStream_t)stream;
   if (pf_empty) {
     return head_dim == 128
@@ -902,7 +903,12 @@ int pa_mixed_step(void* dec_out, int dec_out_dtype, const void* dec_q, const int
   if (st != PA_OK) return st;
   st = head_dim == 128 ? launch_plan<128>(a, s) : launch_plan<64>(a, s);
   if (st != PA_OK) return st;
-  st = prefill(cap);
+  // Beside the decode, which streams its K/V through L2 at several TB/s, a
+  // line survives in L2 for only some tens of microseconds.  The prefill
+  // therefore deals its heads one at a time: every query tile of a (chunk,
+  // head) lands in the same round, on neighbouring CTAs, and they read that
+  // head's K/V together instead of once per round from HBM.
+  st = prefill(cap, 1);
   if (st != PA_OK) return st;
   a.dep_wait = 0;
   return launch_main_any(a, head_dim, dtype, s);

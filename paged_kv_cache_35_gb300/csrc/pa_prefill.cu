@@ -1106,7 +1106,8 @@ int prefill_check(void* out, int out_dtype, const void* q, const int32_t* cu_q_l
 int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_before,
                    const void* k_pool, const void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
                    int num_chunks, int total_q, int max_q_len, int num_heads, int head_dim, int block_size,
-                   int num_blocks, float scale, int dtype, int32_t* err_flag, int max_ctas, void* stream) {
+                   int num_blocks, float scale, int dtype, int32_t* err_flag, int max_ctas, int head_group,
+                   void* stream) {
   pa::PrefillArgs a;
   CUtensorMap tm_q, tm_k, tm_v;
   bool empty = false;
@@ -1145,11 +1146,14 @@ int prefill_launch(void* out, int out_dtype, const void* q, const int32_t* cu_q_
   // persistent: at most one CTA per SM (shared and tensor memory allow one)
   long long ctas = max_ctas > 0 && max_ctas < sms ? max_ctas : sms;
   if (ctas > n_items) ctas = n_items;
-  // A launch of many rounds deals its heads in groups of at least three
-  // rounds' worth of items, so that the CTAs stream one group's K/V at a time
-  // (it can stay in L2 for the group's other query tiles) instead of every head's.
+  // head_group > 0: the caller's group size.  Otherwise a launch of many
+  // rounds deals its heads in groups of at least three rounds' worth of items,
+  // so that the CTAs stream one group's K/V at a time (it can stay in L2 for
+  // the group's other query tiles) instead of every head's.
   a.head_group = num_heads;
-  if (n_items >= 8 * ctas) {
+  if (head_group > 0) {
+    a.head_group = head_group < num_heads ? head_group : num_heads;
+  } else if (n_items >= 8 * ctas) {
     const long long npairs = (long long)a.qtiles * num_chunks;
     const long long g = (3 * ctas + npairs - 1) / npairs;
     if (g < num_heads) {
@@ -1171,5 +1175,5 @@ extern "C" int pa_prefill_chunk(void* out, int out_dtype, const void* q, const i
   pa_host::Range range("pa_prefill_chunk");
   return pa_host::prefill_launch(out, out_dtype, q, cu_q_lens, ctx_before, k_pool, v_pool, block_tables,
                                  max_blocks_per_seq, num_chunks, total_q, max_q_len, num_heads, head_dim, block_size,
-                                 num_blocks, scale, dtype, err_flag, 0, stream);
+                                 num_blocks, scale, dtype, err_flag, 0, 0, stream);
 }

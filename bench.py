@@ -368,12 +368,14 @@ def shared_prefix_decode_workload(pa, W, dev):
     tables, lens = alloc.block_tables(range(n), mb)
     lens_t = torch.from_numpy(lens)
     unique_blocks = sc.num_blocks - alloc.num_free()
+    group_start, group_prefix = alloc.prefix_groups(range(n))
     w = W.DecodeWorkload(
         name="shared_prefix", num_heads=H, head_dim=D, block_size=B, num_blocks=sc.num_blocks, dtype="f16",
         context_lens=lens_t, new_pos=(lens_t - 1).to(torch.int32), block_tables=torch.from_numpy(tables),
         max_blocks_per_seq=mb, q=sc.q, k_new=W.normal((n, H, D), 31, torch.float16, dev),
         v_new=W.normal((n, H, D), 32, torch.float16, dev), k_pool=kp, v_pool=vp, scale=sc.scale,
-        extra={"unique_kv_bytes": 2 * unique_blocks * H * B * D * 2})
+        extra={"unique_kv_bytes": 2 * unique_blocks * H * B * D * 2,
+               "group_start": torch.from_numpy(group_start), "group_prefix": torch.from_numpy(group_prefix)})
     alloc.close()
     return w
 

@@ -69,6 +69,7 @@ extern "C" {
 #define PA_FLAG_BAD_SLOT 2    /* slot_mapping entry >= num_blocks * block_size */
 #define PA_FLAG_BAD_LENGTH 4  /* context length < 0, > max_context_len, or > table capacity */
 #define PA_FLAG_TIMEOUT 8     /* an mbarrier wait exceeded its time limit */
+#define PA_FLAG_BAD_GROUP 16  /* pa_decode_grouped: a group was not usable; its sequences were decoded whole */
 
 /* Library version (major*10000 + minor*100 + patch). */
 int pa_version(void);
@@ -197,6 +198,51 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
               int max_context_len, int num_seqs, int num_heads, int head_dim, int block_size,
               int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
               int partition_size, int32_t* err_flag, void* stream);
+
+/*
+ * Bytes of device workspace pa_decode_grouped needs for these sizes
+ * (partition_size 0 = the automatic choice above).  0 on bad arguments.
+ */
+size_t pa_decode_grouped_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                         int partition_size);
+
+/*
+ * pa_decode_grouped -- pa_decode for a batch in which groups of sequences
+ * share the blocks of a common prefix: the parallel samples or the beams of
+ * one prompt ([summary] section 6, parallel sampling (Figure 9) and beam
+ * search (Figure 10); [blog] "Prefix Sharing").  The outputs are those of pa_decode (the same
+ * equation; the rounding order differs).  Each shared prefix is read from the
+ * pool once for its whole group instead of once per sequence.
+ * Arguments are those of pa_decode, plus:
+ * group_start: device int32 [num_groups + 1]; group g is sequences
+ *   group_start[g] .. group_start[g+1] - 1 (at most 8, at least 1), so groups
+ *   are disjoint ranges of the batch in order; a sequence outside every group
+ *   is decoded on its own.
+ * group_prefix: device int32 [num_groups], a multiple of 16; the tokens
+ *   [0, group_prefix[g]) of every member of group g are the same K/V: every
+ *   member's table holds the first member's block ids over those tokens'
+ *   blocks, and the prefix is at most every member's context length.  A
+ *   group that breaks a rule (or whose range or size is out of bounds) sets
+ *   PA_FLAG_BAD_GROUP and its members are decoded on their own; the results
+ *   are still correct.  pa_alloc_prefix_groups computes groups from the host
+ *   allocator's tables.
+ * num_groups: >= 0 (0 = pa_decode).
+ * workspace: at least pa_decode_grouped_workspace_bytes(...) bytes.
+ * Launches on `stream`: the planning kernel (as in pa_decode; it also
+ *   validates the groups and lists every sequence's own tokens past its
+ *   group's prefix), then the group kernel, persistent, whose warps take
+ *   first the prefix units (group, head, partition of the prefix: each
+ *   16-token tile's K and V are multiplied with all the group's queries on
+ *   the tensor cores) and then the listed items (one sequence, one head);
+ *   the partitions of each (sequence, head) are merged by log-sum-exp as in
+ *   pa_decode.
+ */
+int pa_decode_grouped(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                      int max_context_len, int num_seqs, int num_heads, int head_dim, int block_size,
+                      int num_blocks, float scale, int dtype, const int32_t* group_start,
+                      const int32_t* group_prefix, int num_groups, void* workspace, size_t workspace_bytes,
+                      int partition_size, int32_t* err_flag, void* stream);
 
 /*
  * pa_decode_static_scratch -- pa_decode without any device allocation by
@@ -458,6 +504,17 @@ int pa_alloc_block_table(const pa_alloc* a, int seq_id, int32_t* out, int cap, i
  * max_blocks_per_seq; ctx_lens_out[i] = its length (either output may be NULL). */
 int pa_alloc_block_tables(const pa_alloc* a, const int* seq_ids, int n, int max_blocks_per_seq,
                           int32_t* tables_out, int32_t* ctx_lens_out);
+/* Groups for pa_decode_grouped over the batch seq_ids[0..n) in that order:
+ * runs of consecutive sequences (at most max_group, 1..8) whose tables start
+ * with the same block.  A run grows while the next sequence shares at least
+ * its first full block with the run's first sequence; its prefix is, in
+ * tokens, the leading blocks that every member holds in common with the first
+ * and has filled (length >= (b + 1) * block_size), rounded down to a multiple
+ * of 16; a run of one has prefix 0.  Writes group_start_out[0..G] (host int32,
+ * room for n + 1) and group_prefix_out[0..G) (room for n), *num_groups_out =
+ * G.  PA_ERR_INVALID_ARG for an unknown id or bad sizes. */
+int pa_alloc_prefix_groups(const pa_alloc* a, const int* seq_ids, int n, int max_group, int32_t* group_start_out,
+                           int32_t* group_prefix_out, int* num_groups_out);
 int pa_alloc_num_free(const pa_alloc* a);
 /* Reference count of block_id (-1 if out of range). */
 int pa_alloc_ref(const pa_alloc* a, int block_id);

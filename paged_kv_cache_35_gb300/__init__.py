@@ -43,6 +43,7 @@ PA_FLAG_BAD_BLOCK = 1
 PA_FLAG_BAD_SLOT = 2
 PA_FLAG_BAD_LENGTH = 4
 PA_FLAG_TIMEOUT = 8
+PA_FLAG_BAD_GROUP = 16
 
 _TORCH_TO_PA = {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.float32: PA_F32}
 
@@ -58,6 +59,9 @@ SIGNATURES = {
     "pa_decode_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
     "pa_decode": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _I, _P, _P], _I),
     "pa_decode_static_scratch": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P], _I),
+    "pa_decode_grouped_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
+    "pa_decode_grouped": ([_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _I, _P, _Z, _I,
+                           _P, _P], _I),
     "pa_prefill_chunk": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P], _I),
     "pa_mixed_step": ([_P, _I, _P, _P, _I, _P, _I, _I, _P, _Z, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I,
                        _I, _I, _F, _I, _I, _P, _P], _I),
@@ -88,6 +92,7 @@ SIGNATURES = {
     "pa_alloc_add_seq_prefix": ([_P, _I, _P, _I, _P], _I),
     "pa_alloc_append_tokens": ([_P, _P, _P, _I, _P, _P, _P], _I),
     "pa_alloc_prefix_stats": ([_P, _P, _P], _I),
+    "pa_alloc_prefix_groups": ([_P, _P, _I, _I, _P, _P, _P], _I),
 }
 
 
@@ -252,6 +257,44 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, max_context_le
         _kv_code(k_pool), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         int(partition_size), _dev(err_flag, "err_flag", torch.int32), _stream(stream))
     _check(st, "pa_decode")
+
+
+def pa_decode_grouped_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size=0) -> int:
+    return int(lib().pa_decode_grouped_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len,
+                                                       partition_size))
+
+
+def decode_grouped_workspace(num_seqs, num_heads, head_dim, max_context_len, partition_size=0, device=None):
+    """A uint8 device tensor big enough for pa_decode_grouped with these sizes."""
+    n = pa_decode_grouped_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size)
+    if n == 0:
+        raise ValueError("bad sizes for the grouped decode workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_decode_grouped(out, q, k_pool, v_pool, block_tables, context_lens, max_context_len, scale, group_start,
+                      group_prefix, workspace, err_flag, partition_size=0, stream=None):
+    """pa_decode with each group's shared prefix read once for the group:
+    sequences group_start[g] .. group_start[g+1]-1 share their first
+    group_prefix[g] tokens (device int32 [G+1] and [G]; see pa.h)."""
+    NB, H, B, D = k_pool.shape
+    S = q.shape[0]
+    if tuple(q.shape) != (S, H, D) or tuple(out.shape) != (S, H, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] < S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [>=S][MB], context_lens [S]")
+    G = group_prefix.numel()
+    if group_start.numel() != G + 1:
+        raise ValueError("group_start must hold num_groups + 1 entries")
+    st = lib().pa_decode_grouped(
+        _dev(out, "out", (torch.float16, torch.bfloat16, torch.float32)), _TORCH_TO_PA[out.dtype],
+        _dev(q, "q", k_pool.dtype), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, D, B, NB, float(scale),
+        _kv_code(k_pool), _dev(group_start, "group_start", torch.int32), _dev(group_prefix, "group_prefix", torch.int32),
+        G, _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), int(partition_size),
+        _dev(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "pa_decode_grouped")
 
 
 def pa_decode_static_scratch(out, q, k_pool, v_pool, block_tables, context_lens, max_context_len, scale, err_flag,
@@ -523,6 +566,18 @@ class BlockAllocator:
         _check(lib().pa_alloc_block_tables(self._h, ids.ctypes.data, n, max_blocks_per_seq, tables.ctypes.data,
                                            lens.ctypes.data), "pa_alloc_block_tables")
         return tables, lens
+
+    def prefix_groups(self, seq_ids, max_group: int = 8):
+        """(group_start int32 [G+1], group_prefix int32 [G]) for pa_decode_grouped
+        over the batch seq_ids, in that order (see pa_alloc_prefix_groups)."""
+        ids = _host_i32(list(seq_ids))
+        n = ids.shape[0]
+        start = np.zeros(n + 1, dtype=np.int32)
+        prefix = np.zeros(max(n, 1), dtype=np.int32)
+        g = ctypes.c_int(0)
+        _check(lib().pa_alloc_prefix_groups(self._h, ids.ctypes.data, n, int(max_group), start.ctypes.data,
+                                            prefix.ctypes.data, ctypes.byref(g)), "pa_alloc_prefix_groups")
+        return start[: g.value + 1].copy(), prefix[: g.value].copy()
 
     def num_free(self) -> int:
         return int(lib().pa_alloc_num_free(self._h))

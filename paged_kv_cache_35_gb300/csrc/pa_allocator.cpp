@@ -348,6 +348,52 @@ int pa_alloc_block_tables(const pa_alloc* a, const int* seq_ids, int n, int max_
   return PA_OK;
 }
 
+// Groups for pa_decode_grouped, from the tables: runs of consecutive listed
+// sequences (at most max_group) whose tables start with the same blocks.  A
+// run grows while the next sequence shares at least its first full block with
+// the run's first sequence; the run's prefix is the leading blocks that every
+// member holds in common with the first and has filled (length at least
+// (b + 1) * block_size), in tokens, rounded down to a multiple of 16.  A run
+// of one sequence has prefix 0.
+int pa_alloc_prefix_groups(const pa_alloc* a, const int* seq_ids, int n, int max_group, int32_t* group_start_out,
+                           int32_t* group_prefix_out, int* num_groups_out) {
+  if (a == nullptr || n < 0 || max_group < 1 || max_group > 8 || num_groups_out == nullptr ||
+      (n > 0 && (seq_ids == nullptr || group_prefix_out == nullptr)) || group_start_out == nullptr)
+    return PA_ERR_INVALID_ARG;
+  std::vector<const pa_alloc::Seq*> sq(n);
+  for (int i = 0; i < n; ++i) {
+    auto it = a->seqs.find(seq_ids[i]);
+    if (it == a->seqs.end()) return PA_ERR_INVALID_ARG;
+    sq[i] = &it->second;
+  }
+  const int64_t B = a->block_size;
+  auto full_blocks = [&](const pa_alloc::Seq& s) { return std::min<int64_t>(s.len / B, (int64_t)s.blocks.size()); };
+  int G = 0;
+  for (int i = 0; i < n;) {
+    const pa_alloc::Seq& first = *sq[i];
+    int64_t common = full_blocks(first);
+    int j = i + 1;
+    while (j < n && j - i < max_group && common > 0) {
+      const pa_alloc::Seq& m = *sq[j];
+      const int64_t lim = std::min(common, full_blocks(m));
+      int64_t c = 0;
+      while (c < lim && m.blocks[c] == first.blocks[c]) ++c;
+      if (c == 0) break;
+      common = c;
+      ++j;
+    }
+    int64_t prefix = j - i > 1 ? common * B : 0;
+    prefix = std::min<int64_t>(prefix, INT32_MAX) / 16 * 16;
+    group_start_out[G] = i;
+    group_prefix_out[G] = (int32_t)prefix;
+    ++G;
+    i = j;
+  }
+  group_start_out[G] = n;
+  *num_groups_out = G;
+  return PA_OK;
+}
+
 int pa_alloc_num_free(const pa_alloc* a) { return a ? a->num_free() : -1; }
 
 int pa_alloc_ref(const pa_alloc* a, int block_id) {

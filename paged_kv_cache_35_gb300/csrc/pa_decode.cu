@@ -54,6 +54,10 @@
 #include <cstdio>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -109,6 +113,14 @@ struct DecodeArgs {
   int32_t* err_flag;
   int dep_wait;    // 1: wait for the planning kernel (launched right before); 0: it completed before the
                    // kernel this one was launched behind
+  // pa_decode_grouped only (num_groups == 0 otherwise): sequences
+  // group_start[g] .. group_start[g+1]-1 share their first group_prefix[g]
+  // tokens; the planning kernel validates each group and leaves in
+  // seq_prefix[s] the tokens of s that the group kernel covers (0 if none).
+  int num_groups;
+  const int32_t* group_start;
+  const int32_t* group_prefix;
+  int32_t* seq_prefix;
 };
 
 template <int D, typename T>
@@ -138,6 +150,47 @@ __device__ __forceinline__ bool length_ok(const DecodeArgs& a, int ctx) {
 // Planning kernel: one CTA.  Lists the (sequence, partition) items, longest
 // first; resets the unit counter and the per-(sequence, head) arrival
 // counters; writes zero rows for empty or invalid sequences.
+constexpr int kGroupMax = 8;  // sequences of a group: the 8 columns of one mma n-block
+
+// One warp per group (warp w of nw takes groups w, w + nw, ...): a group is
+// used when its range lies in [0, S) and holds 1..kGroupMax sequences, its
+// prefix is a multiple of 16 tokens (whole tiles: no tile reads a row past
+// it) and at most every member's context length, and every member's table
+// equals the first member's over the prefix's blocks.  Otherwise
+// PA_FLAG_BAD_GROUP is raised and its members are decoded whole.
+__device__ __forceinline__ void validate_groups(const DecodeArgs& a, int w, int nw, int lane) {
+  const int S = a.num_seqs, B = a.block_size;
+  for (int g = w; g < a.num_groups; g += nw) {
+    const int g0 = __ldg(a.group_start + g), g1 = __ldg(a.group_start + g + 1);
+    const int pre = __ldg(a.group_prefix + g);
+    bool ok = g0 >= 0 && g1 > g0 && g1 <= S && g1 - g0 <= kGroupMax && pre >= 0 && pre % kChunk == 0;
+    if (ok && pre > 0) {
+      const int nblk = (pre + B - 1) / B;
+      if ((long long)nblk > a.max_blocks_per_seq) ok = false;
+      if (ok && lane < g1 - g0) {
+        const int ctx = __ldg(a.context_lens + g0 + lane);
+        if (!length_ok(a, ctx) || pre > ctx) ok = false;
+      }
+      if (ok) {
+        const int32_t* t0 = a.block_tables + (size_t)g0 * a.max_blocks_per_seq;
+        const int n = (g1 - g0 - 1) * nblk;  // (member, block) pairs after the first member
+        for (int i = lane; i < n; i += 32) {
+          const int m = 1 + i / nblk, b = i - (m - 1) * nblk;
+          if (__ldg(a.block_tables + (size_t)(g0 + m) * a.max_blocks_per_seq + b) != __ldg(t0 + b)) ok = false;
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+    } else {
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (!ok) {
+      if (lane == 0) atomicOr(a.err_flag, PA_FLAG_BAD_GROUP);
+      continue;
+    }
+    if (lane < g1 - g0) a.seq_prefix[g0 + lane] = pre;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) {
   griddep_launch_dependents();
@@ -154,14 +207,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
     cur[i] = 0;
   }
   for (int i = tid; i < S * H; i += blockDim.x) a.counters[2 + i] = 0;
+  if (a.num_groups > 0) {
+    for (int s = tid; s < S; s += blockDim.x) a.seq_prefix[s] = 0;
+    __syncthreads();
+    validate_groups(a, tid >> 5, blockDim.x >> 5, tid & 31);
+  }
   __syncthreads();
   // item sizes: full partitions of P tokens, then the last part of each
-  // sequence (1..P tokens)
+  // sequence (1..P tokens); a shared prefix (grouped calls) is not listed:
+  // the group kernel covers it, in partitions 0 .. ceil(prefix / P) - 1
   for (int s = tid; s < S; s += blockDim.x) {
     const int ctx = __ldg(a.context_lens + s);
     if (!length_ok(a, ctx) || ctx == 0) continue;
-    const int nfull = (ctx - 1) / P;
-    const int last = ctx - nfull * P;
+    const int rest = ctx - (a.num_groups > 0 ? a.seq_prefix[s] : 0);
+    if (rest == 0) continue;
+    const int nfull = (rest - 1) / P;
+    const int last = rest - nfull * P;
     if (nfull > 0) atomicAdd(&hist[nb - 1], nfull);
     atomicAdd(&hist[(last + kChunk - 1) / kChunk - 1], 1);
   }
@@ -183,15 +244,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
       for (int i = 0; i < H * D; ++i) store_out(a.out, (size_t)s * H * D + i, a.out_dtype, 0.f);
       continue;
     }
-    const int nfull = (ctx - 1) / P;
-    const int last = ctx - nfull * P;
-    const int nparts = nfull + 1;
+    const int skip = a.num_groups > 0 ? a.seq_prefix[s] : 0;
+    const int np0 = (skip + P - 1) / P;  // partitions of the shared prefix
+    const int rest = ctx - skip;
+    if (rest == 0) continue;
+    const int nfull = (rest - 1) / P;
+    const int last = rest - nfull * P;
+    const int nparts = np0 + nfull + 1;
     if (nfull > 0) {
       const int base = offs[nb - 1] + atomicAdd(&cur[nb - 1], nfull);
-      for (int p = 0; p < nfull; ++p) a.items[base + p] = make_int4(s, p, p * P, P | (nparts << 11));
+      for (int p = 0; p < nfull; ++p) a.items[base + p] = make_int4(s, np0 + p, skip + p * P, P | (nparts << 11));
     }
     const int bkt = (last + kChunk - 1) / kChunk - 1;
-    a.items[offs[bkt] + atomicAdd(&cur[bkt], 1)] = make_int4(s, nfull, nfull * P, last | (nparts << 11));
+    a.items[offs[bkt] + atomicAdd(&cur[bkt], 1)] =
+        make_int4(s, np0 + nfull, skip + nfull * P, last | (nparts << 11));
   }
   // Launched as a programmatic dependent of the kernel before it (which may
   // still be running, e.g. the slot scatter writing the pool): finish only
@@ -314,7 +380,7 @@ __device__ __forceinline__ bool publish_unit(const DecodeArgs& a, DecodeSmem<D, 
   }
   const int item = u / H;
   const int h = u - item * H;
-  const int4 it = __ldg(a.items + item);
+  const int4 it = __ldcg(a.items + item);  // written by the planning kernel: coherent load
   const int s = it.x;
   const int tok0 = it.z;
   const int ntok = it.w & 2047;
@@ -343,7 +409,7 @@ template <int D, typename T>
 __device__ __forceinline__ void run_scheduler(const DecodeArgs& a, DecodeSmem<D, T>& sm, int lane) {
   volatile int* abort_flag = &sm.abort_flag;
   const int H = a.num_heads;
-  const long long total_units = (long long)__ldg(a.counters + 1) * H;
+  const long long total_units = (long long)__ldcg(a.counters + 1) * H;
   int published = 0;  // real units published
   bool more = true;
   while (more && published < kUnitQueue) {
@@ -565,6 +631,386 @@ __global__ void __launch_bounds__(kDecodeThreads, PA_DECODE_MIN_CTAS) decode_ker
   }
 }
 
+// ---------------------------------------------------------------------------------
+// Group kernel (pa_decode_grouped): the shared prefix of a group of up to 8
+// sequences (parallel samples or beams of one prompt, whose tables hold the
+// same blocks there) is read once for all of them.  Persistent: each warp
+// takes units from a counter, first the prefix units (group, head, prefix
+// partition of P tokens), then the planned items of every sequence's own
+// tokens (one unit per item and head, one query column), and streams the
+// unit's 16-token K/V tiles through kGSlots ring slots of its own, issuing
+// the tensor copies itself.  Per tile, with the unit's queries as the 8
+// columns of an mma n-block (warp-level m16n8k16 products, fp32 accumulation):
+//   S^T[16 tokens][8 queries] = K_tile . Q^T       (head_dim / 16 products)
+//   online softmax per query (column), P^T rounded to the pool's type
+//   O^T[D][8] += V_tile^T . P^T                    (head_dim / 16 products)
+// P^T leaves the products' accumulator layout (token rows) for their B
+// operand layout (query columns) through an 8x8 register transpose
+// (movmatrix).  A bf16 P is two parts, P_hi + P_lo, as in the prefill, so
+// that the weights carry ~16 bits; an fp16 P is one.  A unit writes each
+// column's normalised partial (max, sum, o) into the partial arrays, and
+// whichever partition of a (sequence, head) arrives last merges them all; a
+// sequence whose tokens form one partition gets its output row directly.
+constexpr int kGWarps = 4;   // units per CTA
+constexpr int kGSlots = 3;   // ring slots per warp
+constexpr int kGHalfBytes = kChunk * 128;  // 16 rows x 64 columns of 2 bytes, 128-byte swizzled
+
+template <int D>
+struct GroupSmem {
+  uint8_t ring[kGWarps][kGSlots][2][D / 64][kGHalfBytes];  // [warp][slot][K, V][64-column half]
+  uint64_t full[kGWarps][kGSlots];
+};
+
+__device__ __forceinline__ void g_tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <typename T>
+__device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1);
+template <>
+__device__ __forceinline__ void mma_16816<__half>(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma_16816<__nv_bfloat16>(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two weights of one token row (queries 2c, 2c+1) rounded to the pool's type,
+// packed low/high; *rest gets what rounding left (the bf16 second part).
+template <typename T>
+__device__ __forceinline__ uint32_t pack_p(float p0, float p1, float* r0, float* r1);
+template <>
+__device__ __forceinline__ uint32_t pack_p<__half>(float p0, float p1, float* r0, float* r1) {
+  const __half2 h = __floats2half2_rn(p0, p1);
+  *r0 = __low2float(h);  // the rounded values (their sum is the row sum)
+  *r1 = __high2float(h);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack_p<__nv_bfloat16>(float p0, float p1, float* r0, float* r1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+  *r0 = p0 - __low2float(h);  // the remainders, for P_lo
+  *r1 = p1 - __high2float(h);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float x0, float x1);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float x0, float x1) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float x0, float x1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kGWarps * 32) group_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                             const __grid_constant__ CUtensorMap tm_v,
+                                                             const DecodeArgs a, int prefix_parts) {
+  constexpr int kHalves = D / 64;
+  constexpr int kKSteps = D / 16;
+  constexpr bool kTwoPart = std::is_same<T, __nv_bfloat16>::value;
+  constexpr uint32_t kSlotTx = 2u * kHalves * kGHalfBytes;
+  static_assert(kMaxPartition / kChunk <= 64, "two block ids per lane");
+  extern __shared__ uint8_t group_smem_raw[];
+  auto& sm = *reinterpret_cast<GroupSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(group_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    for (int i = 0; i < kGSlots; ++i) mbar_init(&sm.full[warp][i], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  // The planning kernel (launched right before) has completed from here on.
+  // Its output (the work list, the counters, the prefixes) is read with
+  // coherent loads: it was written during this grid's lifetime, which the
+  // read-only cache path does not allow for.
+  griddep_wait();
+
+  const int H = a.num_heads, P = a.partition_size, S = a.num_seqs, B = a.block_size;
+  const long long n_prefix = (long long)a.num_groups * H * prefix_parts;
+  const long long total = n_prefix + (long long)__ldcg(a.counters + 1) * H;  // + the planned items, per head
+  // lane's rows of an m16n8 accumulator: r0 = lane / 4 and r0 + 8; its
+  // columns: c0 = 2 (lane % 4) and c0 + 1
+  const int r0 = lane >> 2;
+  const int c0 = 2 * (lane & 3);
+  // ldmatrix row addresses: lane i feeds matrix i / 8, its row i % 8
+  const int lr = (lane & 7) + ((lane >> 3) & 1) * 8;  // K: row (token) of matrices 0..3
+  const int lc = lane >> 4;                          // K: second 8 columns for matrices 2, 3
+  const int vr = (lane & 7) + (lane >> 4) * 8;        // V (transposed load): token row
+  const int vc = (lane >> 3) & 1;                     // V: second 8 dimensions for matrices 1, 3
+  uint32_t x0 = 0;  // tiles this warp has streamed so far: slot and phase of tile j are those of x0 + j
+
+  for (;;) {
+    int uu = 0;
+    if (lane == 0) uu = atomicAdd(a.counters, 1);
+    const long long u = __shfl_sync(0xffffffffu, uu, 0);
+    if (u >= total) break;
+    // the unit: queries (columns) of sequences g0 .. g0+gn-1, head h, tokens
+    // [tok0, tok0 + ntok) of g0's table, partial index p of nparts
+    int g0, gn, h, tok0, ntok, p, nparts;  // nparts: 0 = per member (a shared prefix)
+    if (u < n_prefix) {
+      const int g = (int)(u / ((long long)H * prefix_parts));
+      const int r = (int)(u - (long long)g * H * prefix_parts);
+      h = r / prefix_parts;
+      p = r - h * prefix_parts;
+      g0 = __ldg(a.group_start + g);
+      const int g1 = __ldg(a.group_start + g + 1);
+      if (g0 < 0 || g0 >= S || g1 <= g0 || g1 > S || g1 - g0 > kGroupMax) continue;
+      const int prefix = __ldcg(a.seq_prefix + g0);  // 0 unless the planning kernel accepted the group
+      tok0 = p * P;
+      if (tok0 >= prefix) continue;
+      gn = g1 - g0;
+      ntok = min(P, prefix - tok0);
+      nparts = 0;
+    } else {  // a planned item: one sequence's own tokens, a one-column unit
+      const long long v = u - n_prefix;
+      const int4 it = __ldcg(a.items + v / H);
+      h = (int)(v - (v / H) * H);
+      g0 = it.x;
+      gn = 1;
+      p = it.y;
+      tok0 = it.z;
+      ntok = it.w & 2047;
+      nparts = it.w >> 11;
+    }
+    const int ntiles = (ntok + kChunk - 1) / kChunk;
+    const int32_t* trow = a.block_tables + (size_t)g0 * a.max_blocks_per_seq;
+
+    // the queries: B operand of S^T = K Q^T, column n = lane / 4 (member n),
+    // rows (dimensions) 16 kk + 2 (lane % 4) + {0, 1} and + 8
+    uint32_t qb[kKSteps][2];
+    {
+      const int n = lane >> 2;
+      const T* qrow = static_cast<const T*>(a.q) + ((size_t)(g0 + n) * H + h) * D + c0;
+#pragma unroll
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        qb[kk][0] = n < gn ? __ldg(reinterpret_cast<const unsigned int*>(qrow + 16 * kk)) : 0u;
+        qb[kk][1] = n < gn ? __ldg(reinterpret_cast<const unsigned int*>(qrow + 16 * kk + 8)) : 0u;
+      }
+    }
+    // the unit's block ids, tile j's in lane j % 32 of blk_r[j / 32], read
+    // once up front so that no copy waits on a table read
+    int32_t blk_r[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int j = lane + 32 * r;
+      blk_r[r] = j < ntiles ? __ldg(trow + (tok0 + j * kChunk) / B) : -1;
+    }
+    uint32_t bad = 0;  // bit s: slot s holds no data
+    auto issue = [&](int j) {
+      const int s = (int)((x0 + j) % kGSlots);
+      const int tok = tok0 + j * kChunk;
+      const int32_t blk = __shfl_sync(0xffffffffu, (j >> 5) ? blk_r[1] : blk_r[0], j & 31);
+      if (blk >= 0 && blk < a.num_blocks) {
+        bad &= ~(1u << s);
+        if (lane == 0) {
+          const int row = (int)(((long long)blk * H + h) * B + tok % B);
+          uint64_t* bar = &sm.full[warp][s];
+          mbar_arrive_expect_tx(bar, kSlotTx);
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf) {
+            g_tma_load_2d(smem_u32(sm.ring[warp][s][0][hf]), &tm_k, 64 * hf, row, bar);
+            g_tma_load_2d(smem_u32(sm.ring[warp][s][1][hf]), &tm_v, 64 * hf, row, bar);
+          }
+        }
+      } else {
+        bad |= 1u << s;
+        if (lane == 0) {
+          atomicOr(a.err_flag, PA_FLAG_BAD_BLOCK);
+          mbar_arrive(&sm.full[warp][s]);
+        }
+      }
+    };
+    for (int j = 0; j < ntiles && j < kGSlots; ++j) issue(j);
+
+    float m[2] = {-INFINITY, -INFINITY};  // running max per column (query), log2 units
+    float l[2] = {0.f, 0.f};              // this lane's part of the column sums
+    float o[kKSteps][4];                  // O^T: rows 16 mb + r0 (+8) = dimensions, columns = queries
+#pragma unroll
+    for (int mb = 0; mb < kKSteps; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
+
+    int j_abort = -1;  // the tile whose wait gave up
+    for (int j = 0; j < ntiles; ++j) {
+      const uint32_t x = x0 + j;
+      const int s = (int)(x % kGSlots);
+      const bool ok = mbar_wait(&sm.full[warp][s], (x / kGSlots) & 1, nullptr, a.err_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        j_abort = j;
+        break;
+      }
+      const int valid = ntok - j * kChunk;  // rows of this tile inside the unit (>= 1)
+      if (!((bad >> s) & 1u)) {
+        const uint32_t kbase = smem_u32(sm.ring[warp][s][0][0]);
+        const uint32_t vbase = smem_u32(sm.ring[warp][s][1][0]);
+        if (valid < kChunk) {
+          // V rows past the sequence's end may hold any bits (even NaN), and
+          // a zero weight times NaN is NaN: clear them before the product
+          const int per_half = (kChunk - valid) * 8;
+          for (int i = lane; i < per_half * kHalves; i += 32) {
+            const int hf = i / per_half, rem = i - hf * per_half;
+            const int row = valid + (rem >> 3);
+            *reinterpret_cast<uint4*>(sm.ring[warp][s][1][hf] + row * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();  // before the slot's next tensor copy overwrites these bytes
+          __syncwarp();
+        }
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; ++kk) {
+          const int hf = kk >> 2, ch = (kk & 3) * 2 + lc;
+          uint32_t af[4];
+          ldsm_x4(kbase + hf * kGHalfBytes + lr * 128 + ((ch ^ (lr & 7)) << 4), af);
+          mma_16816<T>(c, af, qb[kk][0], qb[kk][1]);
+        }
+        // scores in log2 units; rows past the unit do not count
+        float sc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = (r0 + 8 * (e >> 1)) < valid ? c[e] * a.qscale : -INFINITY;
+        float tmax[2] = {fmaxf(sc[0], sc[2]), fmaxf(sc[1], sc[3])};
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+          tmax[0] = fmaxf(tmax[0], __shfl_xor_sync(0xffffffffu, tmax[0], sh));
+          tmax[1] = fmaxf(tmax[1], __shfl_xor_sync(0xffffffffu, tmax[1], sh));
+        }
+        float alpha[2], pr[4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float mn = fmaxf(m[q], tmax[q]);
+          alpha[q] = mn == -INFINITY ? 1.f : exp2f(m[q] - mn);
+          m[q] = mn;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[e] = m[e & 1] == -INFINITY ? 0.f : exp2f(sc[e] - m[e & 1]);
+        float rest[4];
+        const uint32_t p01 = pack_p<T>(pr[0], pr[1], &rest[0], &rest[1]);
+        const uint32_t p23 = pack_p<T>(pr[2], pr[3], &rest[2], &rest[3]);
+        if (kTwoPart) {
+          l[0] = l[0] * alpha[0] + (pr[0] + pr[2]);
+          l[1] = l[1] * alpha[1] + (pr[1] + pr[3]);
+        } else {  // the rounded weights
+          l[0] = l[0] * alpha[0] + (rest[0] + rest[2]);
+          l[1] = l[1] * alpha[1] + (rest[1] + rest[3]);
+        }
+        // P^T as the B operand: column n = lane / 4 (query), rows = tokens
+        const uint32_t b0 = movmatrix_trans(p01), b1 = movmatrix_trans(p23);
+        uint32_t b0l = 0, b1l = 0;
+        if (kTwoPart) {
+          b0l = movmatrix_trans(pack2<T>(rest[0], rest[1]));
+          b1l = movmatrix_trans(pack2<T>(rest[2], rest[3]));
+        }
+#pragma unroll
+        for (int mb = 0; mb < kKSteps; ++mb) {
+          o[mb][0] *= alpha[0];
+          o[mb][1] *= alpha[1];
+          o[mb][2] *= alpha[0];
+          o[mb][3] *= alpha[1];
+          const int ch = 2 * mb + vc, hf = ch >> 3, cin = ch & 7;
+          uint32_t af[4];
+          ldsm_x4_trans(vbase + hf * kGHalfBytes + vr * 128 + ((cin ^ (vr & 7)) << 4), af);
+          mma_16816<T>(o[mb], af, b0, b1);
+          if (kTwoPart) mma_16816<T>(o[mb], af, b0l, b1l);
+        }
+      }
+      __syncwarp();  // every lane's reads of the slot are done
+      if (j + kGSlots < ntiles) issue(j + kGSlots);
+    }
+    if (j_abort >= 0) {  // tiles j_abort .. j_abort + kGSlots - 1 were issued: let them land before exit
+      if (lane == 0)
+        for (int t = j_abort; t < ntiles && t < j_abort + kGSlots; ++t)
+          mbar_wait_drain(&sm.full[warp][(x0 + t) % kGSlots], ((x0 + t) / kGSlots) & 1);
+      return;
+    }
+    x0 += (uint32_t)ntiles;
+
+    // column sums over the 8 lanes of each column pair
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], sh);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], sh);
+    }
+    if (nparts == 1) {  // a sequence whose tokens form one partition: its output row
+      if (c0 == 0) {
+        const float inv = l[0] > 0.f ? 1.f / l[0] : 0.f;
+        const size_t ob = ((size_t)g0 * H + h) * D;
+#pragma unroll
+        for (int mb = 0; mb < kKSteps; ++mb) {
+          store_out(a.out, ob + 16 * mb + r0, a.out_dtype, o[mb][0] * inv);
+          store_out(a.out, ob + 16 * mb + r0 + 8, a.out_dtype, o[mb][2] * inv);
+        }
+      }
+      continue;
+    }
+    // each member's normalised partial for partition p
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int n = c0 + q;
+      if (n >= gn) continue;
+      const size_t pidx = ((size_t)(g0 + n) * H + h) * a.max_parts + p;
+      const float inv = l[q] > 0.f ? 1.f / l[q] : 0.f;
+      float* po = a.part_o + pidx * D;
+#pragma unroll
+      for (int mb = 0; mb < kKSteps; ++mb) {
+        po[16 * mb + r0] = o[mb][q] * inv;
+        po[16 * mb + r0 + 8] = o[mb][q + 2] * inv;
+      }
+      if (r0 == 0) a.part_ml[pidx] = make_float2(m[q], l[q]);
+    }
+    __threadfence();
+    __syncwarp();
+    for (int n = 0; n < gn; ++n) {
+      const int s = g0 + n;
+      int np = nparts;
+      if (np == 0) {  // a member of a shared prefix: its prefix partitions, then its own
+        const int prefix = __ldcg(a.seq_prefix + g0);
+        const int rest = __ldg(a.context_lens + s) - prefix;
+        np = (prefix + P - 1) / P + (rest > 0 ? (rest + P - 1) / P : 0);
+      }
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(&a.counters[2 + s * H + h], 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == np - 1) {  // every partition of (s, h) is in: merge them
+        __threadfence();
+        merge_partitions<D>(a, s, h, np, lane);
+      }
+    }
+  }
+}
+
 }  // namespace pa
 
 // ---------------------------------------------------------------------------------
@@ -753,7 +1199,95 @@ int decode_setup(void* out, int out_dtype, const void* q, const void* k_pool, co
   a.part_o = reinterpret_cast<float*>(ws + w.o);
   a.err_flag = err_flag;
   a.dep_wait = 1;
+  a.num_groups = 0;
+  a.group_start = nullptr;
+  a.group_prefix = nullptr;
+  a.seq_prefix = nullptr;
   return PA_OK;
+}
+
+// pa_decode_grouped's workspace: pa_decode's with one more partition per
+// sequence (a shared prefix ends mid-partition at most once), then the
+// validated prefix length of every sequence.
+struct GroupedLayout {
+  WsLayout base;
+  size_t seq_prefix, total;
+};
+
+GroupedLayout grouped_layout(int S, int H, int D, int max_parts) {
+  GroupedLayout g;
+  g.base = ws_layout(S, H, D, max_parts + 1);
+  g.seq_prefix = g.base.total;
+  g.total = align_up(g.seq_prefix + sizeof(int32_t) * (size_t)S, 256);
+  return g;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A pool [num_blocks][heads][block][head_dim] as rows of head_dim elements;
+// a copy is 16 rows of one 64-column half, 128-byte swizzled.
+int encode_pool_map(CUtensorMap* m, const void* pool, int dtype, int head_dim, uint64_t rows) {
+  auto encode = tensor_map_encoder();
+  if (encode == nullptr) return PA_ERR_CUDA;
+  const CUtensorMapDataType tdt = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)pa::kChunk};
+  cuuint32_t es[2] = {1, 1};
+  return encode(m, tdt, 2, const_cast<void*>(pool), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+// The group kernel, a persistent grid of as many CTAs as fit on the SMs,
+// launched as a programmatic dependent of the planning kernel: its CTAs set
+// up while the planning finishes and wait for it (griddepcontrol.wait) before
+// reading anything the planning writes.
+template <int D, typename T>
+int launch_group(const pa::DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int prefix_parts,
+                 cudaStream_t stream) {
+  const int smem = (int)sizeof(pa::GroupSmem<D>) + 1024;  // + room to align the ring to 1024 bytes
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  static std::atomic<int> occupancy[64];  // resident CTAs per SM, per device (0: not configured)
+  int occ = occupancy[dev].load(std::memory_order_acquire);
+  if (occ == 0) {
+    if (cudaFuncSetAttribute(pa::group_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pa::group_kernel<D, T>, pa::kGWarps * 32, smem) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    if (occ < 1) occ = 1;
+    occupancy[dev].store(occ, std::memory_order_release);
+  }
+  const int sms = pa_host::device_sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sms * occ));
+  cfg.blockDim = dim3(pa::kGWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // setup overlaps the planning kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa::group_kernel<D, T>, tk, tv, a, prefix_parts) == cudaSuccess ? PA_OK
+                                                                                                 : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -830,6 +1364,87 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_pool, const
     return dtype == PA_F16 ? launch_decode<128, __half>(a, s) : launch_decode<128, __nv_bfloat16>(a, s);
   }
   return dtype == PA_F16 ? launch_decode<64, __half>(a, s) : launch_decode<64, __nv_bfloat16>(a, s);
+}
+
+size_t pa_decode_grouped_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                         int partition_size) {
+  if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+  const int P = resolve_partition(num_seqs, num_heads, max_context_len, partition_size);
+  if (P < pa::kChunk || P > pa::kMaxPartition || P % pa::kChunk != 0) return 0;
+  const int max_parts = decode_max_parts(max_context_len, P);
+  if (max_parts + 1 >= kMaxPartsPerSeq) return 0;
+  return grouped_layout(num_seqs, num_heads, head_dim, max_parts).total;
+}
+
+// pa_decode_grouped: pa_decode for a batch in which groups of sequences share
+// a prompt's blocks (parallel sampling and beam search, [summary] section 6,
+// Figures 9-10, and [blog] "Prefix Sharing"): the planning kernel (which
+// validates the groups and lists every sequence's own tokens as items), then
+// the group kernel, which reads each shared prefix once for its whole group
+// and streams the items too.
+int pa_decode_grouped(void* out, int out_dtype, const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                      int max_context_len, int num_seqs, int num_heads, int head_dim, int block_size,
+                      int num_blocks, float scale, int dtype, const int32_t* group_start,
+                      const int32_t* group_prefix, int num_groups, void* workspace, size_t workspace_bytes,
+                      int partition_size, int32_t* err_flag, void* stream) {
+  pa_host::Range range("pa_decode_grouped");
+  if (num_groups < 0 || (num_groups > 0 && (group_start == nullptr || group_prefix == nullptr)))
+    return PA_ERR_INVALID_ARG;
+  pa::DecodeArgs a;
+  bool empty = false;
+  int st = decode_setup(out, out_dtype, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                        max_context_len, num_seqs, num_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
+                        workspace_bytes, partition_size, err_flag, a, empty);
+  if (st != PA_OK || empty) return st;
+  const int prefix_parts = a.max_parts;  // a group's prefix is at most max_context_len tokens
+  if (prefix_parts + 1 >= kMaxPartsPerSeq) return PA_ERR_UNSUPPORTED;
+  // the group kernel counts its units (prefix units, then items x heads) in an int
+  if ((long long)num_groups * num_heads * prefix_parts + (long long)num_seqs * (prefix_parts + 1) * num_heads >=
+      (1ll << 31))
+    return PA_ERR_UNSUPPORTED;
+  const GroupedLayout gl = grouped_layout(num_seqs, num_heads, head_dim, a.max_parts);
+  if (workspace_bytes < gl.total) return PA_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  a.max_parts += 1;
+  a.counters = reinterpret_cast<int*>(ws + gl.base.counters);
+  a.items = reinterpret_cast<int4*>(ws + gl.base.items);
+  a.part_ml = reinterpret_cast<float2*>(ws + gl.base.ml);
+  a.part_o = reinterpret_cast<float*>(ws + gl.base.o);
+  a.num_groups = num_groups;
+  a.group_start = group_start;
+  a.group_prefix = group_prefix;
+  a.seq_prefix = reinterpret_cast<int32_t*>(ws + gl.seq_prefix);
+  if (pa_host::debug_checks()) {
+    int64_t bad[2];
+    st = pa_host::check_decode_inputs(block_tables, max_blocks_per_seq, context_lens, num_seqs, max_context_len,
+                                      block_size, num_blocks, stream, bad);
+    if (st != PA_OK) {
+      std::fprintf(stderr, "pa_decode_grouped (PA_DEBUG): sequence %lld, logical block %lld is invalid\n",
+                   (long long)bad[0], (long long)bad[1]);
+      return st;
+    }
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (num_groups == 0) {
+    return head_dim == 128
+               ? (dtype == PA_F16 ? launch_decode<128, __half>(a, s) : launch_decode<128, __nv_bfloat16>(a, s))
+               : (dtype == PA_F16 ? launch_decode<64, __half>(a, s) : launch_decode<64, __nv_bfloat16>(a, s));
+  }
+  const uint64_t pool_rows = (uint64_t)num_blocks * num_heads * block_size;
+  if (pool_rows >= (1ull << 31)) return PA_ERR_INVALID_ARG;
+  CUtensorMap tk, tv;
+  st = encode_pool_map(&tk, k_pool, dtype, head_dim, pool_rows);
+  if (st == PA_OK) st = encode_pool_map(&tv, v_pool, dtype, head_dim, pool_rows);
+  if (st != PA_OK) return st;
+  st = configure_any(head_dim, dtype);
+  if (st != PA_OK) return st;
+  st = head_dim == 128 ? launch_plan<128>(a, s) : launch_plan<64>(a, s);
+  if (st != PA_OK) return st;
+  return head_dim == 128 ? (dtype == PA_F16 ? launch_group<128, __half>(a, tk, tv, prefix_parts, s)
+                                            : launch_group<128, __nv_bfloat16>(a, tk, tv, prefix_parts, s))
+                         : (dtype == PA_F16 ? launch_group<64, __half>(a, tk, tv, prefix_parts, s)
+                                            : launch_group<64, __nv_bfloat16>(a, tk, tv, prefix_parts, s));
 }
 
 // pa_mixed_step: one step of a batch that mixes decode sequences and prefill

@@ -272,6 +272,81 @@ def test_beam_search_fork_and_prune_match_model(pa):
         alloc.close()
 
 
+def test_prefix_groups_follow_the_tables(pa):
+    """pa_alloc_prefix_groups on beam-search states: the groups cover the
+    batch in order, hold 1..max_group sequences, and their prefixes are
+    multiples of 16 within every member's length over which every member's
+    table equals the first member's; the run rule (extend while the next
+    sequence shares a full leading block; prefix = the common filled leading
+    blocks) is restated here from its definition."""
+    rng = random.Random(5)
+    for width, B, max_group in ((8, 16, 8), (5, 4, 3), (6, 32, 8), (4, 1, 2)):
+        model = BlockAllocatorModel(600, B)
+        alloc = pa.BlockAllocator(600, B)
+        for m in (model, alloc):
+            m.add_seq(0)
+        for _ in range(70):
+            model.append_slots([0])
+            alloc.append_slots([0])
+        beams, nxt = [0], 1
+        for step in range(12):
+            parents = [rng.choice(beams) for _ in range(width)]
+            new = list(range(nxt, nxt + width))
+            nxt += width
+            for p_, c in zip(parents, new):
+                model.fork(p_, c)
+                alloc.fork(p_, c)
+            for b in beams:
+                model.free_seq(b)
+                alloc.free_seq(b)
+            for _ in range(rng.randint(1, 9)):
+                model.append_slots(new)
+                alloc.append_slots(new)
+            beams = new
+            order = beams[:]
+            rng.shuffle(order)
+            starts, prefixes = alloc.prefix_groups(order, max_group)
+            tables = [model.table(s) for s in order]
+            lens = [model.length(s) for s in order]
+            # the run rule, restated
+            want_s, want_p, i = [0], [], 0
+            while i < len(order):
+                def full(k):
+                    return min(lens[k] // B, len(tables[k]))
+                common, j = full(i), i + 1
+                while j < len(order) and j - i < max_group and common > 0:
+                    c, lim = 0, min(common, full(j))
+                    while c < lim and tables[j][c] == tables[i][c]:
+                        c += 1
+                    if c == 0:
+                        break
+                    common, j = c, j + 1
+                want_p.append((common * B if j - i > 1 else 0) // 16 * 16)
+                want_s.append(j)
+                i = j
+            assert starts.tolist() == want_s and prefixes.tolist() == want_p
+            # what pa_decode_grouped requires of a group
+            for g in range(len(prefixes)):
+                g0, g1, pre = int(starts[g]), int(starts[g + 1]), int(prefixes[g])
+                assert 1 <= g1 - g0 <= max_group and pre % 16 == 0
+                nb = -(-pre // B)
+                for k in range(g0, g1):
+                    assert pre <= lens[k] and tables[k][:nb] == tables[g0][:nb]
+        alloc.close()
+    with pytest.raises(pa.PAError):
+        pa.BlockAllocator(8, 16).prefix_groups([3])  # unknown sequence
+
+
+def test_grouped_workspace_sizes(pa):
+    for S, H, D, mx in ((64, 40, 128, 1256), (4, 4, 64, 46), (256, 32, 128, 16384)):
+        plain = pa.pa_decode_workspace_bytes(S, H, D, mx, 0)
+        grouped = pa.pa_decode_grouped_workspace_bytes(S, H, D, mx, 0)
+        parts = -(-mx // pa.pa_decode_partition_size(S, H, mx)) + 1  # a prefix adds at most one partition
+        assert grouped > plain and grouped >= 4 * S * H * parts * (D + 2) + 4 * S and grouped % 256 == 0
+    assert pa.pa_decode_grouped_workspace_bytes(4, 4, 64, 100, 24) == 0
+    assert pa.pa_decode_grouped_workspace_bytes(1, 1, 128, (1 << 24) - 16, 16) == 0  # 2^20 partitions with the extra
+
+
 def test_allocator_errors(pa):
     a = pa.BlockAllocator(2, 4)
     a.add_seq(0)

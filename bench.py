@@ -45,7 +45,9 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, from an ncu capture of one launch (dram__bytes_read.sum +
 # dram__bytes_write.sum); valid only for the decode kernel source whose
 # sha256 prefix is given (otherwise reported as null).
-TRAFFIC = {"bytes_per_launch": 1488302592, "kernel_sha256_prefix": "71fdb188290db9f5"}
+TRAFFIC = {"bytes_per_launch": 1488319232, "kernel_sha256_prefix": "b3c62dda8d40ca1e"}
+# The group kernel (pa_decode_grouped) on the parallel-sampling workload: DRAM bytes of one launch.
+GROUP_TRAFFIC = {"bytes_per_launch": 348896512, "kernel_sha256_prefix": "b3c62dda8d40ca1e"}
 
 
 # DRAM bytes (read + write) per pa_prefill_chunk call on the four-prompt
@@ -91,6 +93,22 @@ def decode_bytes(ctx_lens, H, D, B, elt) -> int:
     qo = 2 * len(ctx_lens) * H * D * elt
     tables = 4 * sum(-(-int(c) // B) for c in ctx_lens)
     return kv + qo + tables + 4 * len(ctx_lens)
+
+
+def grouped_decode_bytes(ctx_lens, starts, prefixes, H, D, B, elt) -> int:
+    """Algorithmic bytes of one pa_decode_grouped call: each group's shared
+    prefix K and V once per group, every sequence's own K and V, q and out
+    rows, the table entries read (the prefix's once per group), the context
+    lengths and the group arrays."""
+    ctx = [int(c) for c in ctx_lens]
+    pre = [0] * len(ctx)
+    for g, p in enumerate(prefixes):
+        for s in range(int(starts[g]), int(starts[g + 1])):
+            pre[s] = int(p)
+    kv = 2 * (sum(int(p) for p in prefixes) + sum(c - q for c, q in zip(ctx, pre))) * H * D * elt
+    qo = 2 * len(ctx) * H * D * elt
+    tables = 4 * (sum(-(-int(p) // B) for p in prefixes) + sum(-(-c // B) - q // B for c, q in zip(ctx, pre)))
+    return kv + qo + tables + 4 * len(ctx) + 4 * (2 * len(prefixes) + 1)
 
 
 def scatter_bytes(T, H, D, elt) -> int:
@@ -581,13 +599,25 @@ def measure_decode(args, rank, world, local, name, secondary=False):
     ws = pa.decode_workspace(S, H, D, mx, device=dev)
     err = pa.new_error_flag(dev)
     stream = torch.cuda.current_stream(dev)
+    # parallel sampling: the step decodes with each shared prompt read once per group
+    grouped = "group_start" in w.extra
+    if grouped:
+        gs_d, gp_d = w.extra["group_start"].to(dev), w.extra["group_prefix"].to(dev)
+        ws_g = pa.decode_grouped_workspace(S, H, D, mx, device=dev)
+
+    def decode_plain(q_in=None):
+        pa.pa_decode(out, w.q if q_in is None else q_in, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err,
+                     stream=stream)
 
     def prefill():
         pa.pa_prefill_chunk(pout, mixed.chunk_q, cu_d, cb_d, w.k_pool, w.v_pool, ctab_d, mq, w.scale, err, stream)
 
     def decode(q_in=None):
-        pa.pa_decode(out, w.q if q_in is None else q_in, w.k_pool, w.v_pool, tables_d, ctx_d, mx, w.scale, ws, err,
-                     stream=stream)
+        if grouped:
+            pa.pa_decode_grouped(out, w.q if q_in is None else q_in, w.k_pool, w.v_pool, tables_d, ctx_d, mx,
+                                 w.scale, gs_d, gp_d, ws_g, err, stream=stream)
+        else:
+            decode_plain(q_in)
 
     def mixed_step(q_in=None, tables_in=None, ctx_in=None, cq_in=None, cu_in=None, cb_in=None, ctab_in=None):
         pick = lambda given, resident: resident if given is None else given
@@ -609,7 +639,9 @@ def measure_decode(args, rank, world, local, name, secondary=False):
     if flags:
         raise RuntimeError(f"device error flags {flags} during warm-up")
 
-    dbytes = decode_bytes(w.context_lens.tolist(), H, D, B, elt)
+    logical_bytes = decode_bytes(w.context_lens.tolist(), H, D, B, elt)
+    dbytes = (grouped_decode_bytes(w.context_lens.tolist(), w.extra["group_start"].tolist(),
+                                   w.extra["group_prefix"].tolist(), H, D, B, elt) if grouped else logical_bytes)
     sbytes = scatter_bytes(k_new.shape[0], H, D, elt)
     pflops = pbytes = 0
     if mixed is not None:
@@ -655,6 +687,9 @@ def measure_decode(args, rank, world, local, name, secondary=False):
         # it reads per call (>= 1.4 GB on the full-size batches) is far larger than L2.
         dec_t = time_calls(decode, stream, dev, max(K, 100), 50)
         dec_ms = dec_t["mean_ms_back_to_back"]
+        if grouped:  # the same state decoded sequence by sequence, for comparison
+            plain_t = time_calls(decode_plain, stream, dev, max(K, 100), 50)
+            decode()  # `out` holds the grouped result again (the end-to-end check compares bits)
     else:
         # Component pass: scatter, decode, prefill one after the other with
         # events around the two attention calls -- inside the concurrent step
@@ -693,6 +728,7 @@ def measure_decode(args, rank, world, local, name, secondary=False):
     achieved = dbytes / (dec_ms / 1e3) / 1e9
     sha = kernel_sha()
     traffic = (TRAFFIC["bytes_per_launch"] if name == "llama13b" and TRAFFIC["kernel_sha256_prefix"] == sha
+               else GROUP_TRAFFIC["bytes_per_launch"] if grouped and GROUP_TRAFFIC["kernel_sha256_prefix"] == sha
                else None)
     launches = 3 + (1 if mixed is not None else 0)
     line = {
@@ -716,8 +752,20 @@ def measure_decode(args, rank, world, local, name, secondary=False):
         line["roofline"]["note"] = dec_note
     if "unique_kv_bytes" in w.extra:
         line["config"]["unique_kv_bytes"] = w.extra["unique_kv_bytes"]
-        line["roofline"]["note"] = ("logical bytes: shared prompt blocks are counted once per sample that reads "
-                                    "them; the unique K/V footprint is config.unique_kv_bytes")
+    if grouped:
+        line["roofline"]["kernel"] = "pa_decode_grouped call (planning kernel + persistent group kernel)"
+        line["roofline"]["note"] = ("bytes as the grouped call reads them: each shared prompt once per group, "
+                                    "every sample's own tokens once")
+        line["config"]["step"] = ("pa_reshape_and_cache (1 new token/seq) + pa_decode_grouped over ctx (8 groups "
+                                  "of 8 samples, prompt blocks shared)")
+        line["config"]["groups"] = {"group_start": w.extra["group_start"].tolist(),
+                                    "group_prefix": w.extra["group_prefix"].tolist()}
+        line["logical"] = {"bytes_per_step": logical_bytes + sbytes,
+                           "GBs": (logical_bytes + sbytes) * K * world / total_s / 1e9,
+                           "note": "shared prompt blocks counted once per sample that attends over them"}
+        line["ungrouped_decode"] = {"kernel": "pa_decode call on the same state", "calls": plain_t,
+                                    "avg_launch_ms": plain_t["mean_ms_back_to_back"],
+                                    "grouped_speedup": plain_t["mean_ms_back_to_back"] / dec_ms}
     if mixed is not None:
         line["roofline"]["note"] = ("decode kernel timed alone in a component pass after the timed region (inside "
                                     "the concurrent step its events would also span the prefill)")
@@ -774,6 +822,9 @@ def measure_decode(args, rank, world, local, name, secondary=False):
             d_cq, d_cu, d_cb, d_ctab = d_in[6:]
             pa.pa_mixed_step(d_out[0], d_q, d_tables, d_ctx, mx, ws, d_out[1], d_cq, d_cu, d_cb, d_ctab, mq,
                              w.k_pool, w.v_pool, w.scale, err, stream=stream)
+        elif grouped:
+            pa.pa_decode_grouped(d_out[0], d_q, w.k_pool, w.v_pool, d_tables, d_ctx, mx, w.scale, gs_d, gp_d, ws_g,
+                                 err, stream=stream)
         else:
             pa.pa_decode(d_out[0], d_q, w.k_pool, w.v_pool, d_tables, d_ctx, mx, w.scale, ws, err, stream=stream)
         done[b].record(stream)
@@ -816,7 +867,7 @@ OTHER_CONFIGS = ("tiny", "shared_prefix", "long_context", "mixed", "budget512", 
 def secondary_summary(line: dict) -> dict:
     keep = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "roofline", "clocks",
             "seq_steps_per_s", "prefill", "sequential_ms_per_step", "concurrent_speedup_vs_sequential",
-            "gpu_launches", "copy_blocks_roofline", "sweep_by_block_size")
+            "gpu_launches", "copy_blocks_roofline", "sweep_by_block_size", "logical", "ungrouped_decode")
     return {k: line[k] for k in keep if k in line}
 
 

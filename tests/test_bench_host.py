@@ -94,3 +94,20 @@ def test_clock_summary_flags_throttle_reasons():
     assert s["reasons"] == ["sw_power_cap"]
     s = cs.summary(10.0, 11.0)  # no sample inside: falls back to the whole run
     assert s["samples"] == 3 and "hw_slowdown" in s["reasons"]
+
+
+def test_grouped_decode_bytes():
+    """Without shared prefixes the grouped call reads what pa_decode reads
+    (plus the group arrays); a group of n members sharing p tokens reads
+    those tokens' K/V and table entries once instead of n times."""
+    import bench
+
+    ctx, H, D, B, elt = [40, 700, 1029, 16], 3, 128, 16, 2
+    plain = bench.decode_bytes(ctx, H, D, B, elt)
+    assert bench.grouped_decode_bytes(ctx, [0, 4], [0], H, D, B, elt) == plain + 4 * 3
+    ctx = [1000 + 5, 1000 + 200, 1000 + 77]
+    shared = 992
+    got = bench.grouped_decode_bytes(ctx, [0, 3], [shared], H, D, B, elt)
+    saved_kv = 2 * shared * H * D * elt * (3 - 1)
+    saved_tables = 4 * (shared // B) * (3 - 1)
+    assert got == bench.decode_bytes(ctx, H, D, B, elt) - saved_kv - saved_tables + 4 * 3

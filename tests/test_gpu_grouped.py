@@ -286,3 +286,30 @@ def test_parallel_sampling_workload_grouped(pa):
     assert bits_equal(kp, kb) and bits_equal(vp, vb)
     ref = oracle.decode(sc.q, kb, vb, o_tables, o_lens, B, sc.scale, "f16")
     assert_attn_close(out, ref, "f16", "grouped parallel-sampling decode")
+
+
+def test_bad_block_in_a_shared_prefix(pa):
+    """A block id out of range inside a group's shared prefix (in every
+    member's table, so the group stays valid) raises PA_FLAG_BAD_BLOCK and
+    leaves that 16-token tile out of each member's sum; other sequences are
+    untouched."""
+    case = grouped_case([(64, [100, 130]), (32, [50, 60])], H=2, D=128, B=16, dtype="f16", seed=19, singles=(40,))
+    q, kp, vp, tables, ctx, gs, gp = case
+    NB = int(kp.shape[0])
+    bad = tables.clone()
+    bad[0, 1] = NB + 5
+    bad[1, 1] = NB + 5
+    out, flags = grouped_call(pa, (q, kp, vp, bad, ctx, gs, gp))
+    assert flags == pa.PA_FLAG_BAD_BLOCK
+    assert torch.isfinite(out).all()
+    ref = oracle_ref(case, "f16")
+    assert_attn_close(out[2:], ref[2:], "f32", "sequences without the bad entry")
+    # the group's members without their second page: the oracle over the
+    # tables with that entry taken out and 16 fewer tokens
+    kept, shorter = tables.clone(), ctx.clone()
+    for s in (0, 1):
+        row = tables[s].tolist()
+        kept[s] = torch.tensor(row[:1] + row[2:] + row[:1], dtype=kept.dtype)
+        shorter[s] -= 16
+    ref2 = oracle.decode(q, kp, vp, kept, shorter, 16, 1 / np.sqrt(128), "f16")
+    assert_attn_close(out[:2], ref2[:2], "f32", "members whose shared second page is out of range")

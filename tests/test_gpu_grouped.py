@@ -313,3 +313,40 @@ def test_bad_block_in_a_shared_prefix(pa):
         shorter[s] -= 16
     ref2 = oracle.decode(q, kp, vp, kept, shorter, 16, 1 / np.sqrt(128), "f16")
     assert_attn_close(out[:2], ref2[:2], "f32", "members whose shared second page is out of range")
+
+
+N_FUZZ = 60
+
+
+@pytest.mark.parametrize("case", range(N_FUZZ))
+def test_grouped_random_cases(pa, case):
+    """Seeded random layouts: 1-4 groups of 1-8 sequences with prefixes of 0-640
+    tokens (multiples of 16), members ending at the prefix or past it, sequences
+    outside every group (empty ones included), both dtypes, head_dim 64 / 128,
+    block sizes that are multiples of 16, partition lengths, output dtypes; the
+    output starts as NaN so that an unwritten row fails."""
+    rng = np.random.default_rng(3000 + case)
+    D = int(rng.choice([64, 128]))
+    B = int(rng.choice([16, 32, 48, 64, 128, 256]))
+    H = int(rng.integers(1, 6))
+    dtype = str(rng.choice(["f16", "bf16"]))
+    out_dtype = str(rng.choice(["f32", dtype]))
+    P = int(rng.choice([0, 16, 64, 112, 512, 1024]))
+    groups = []
+    for _ in range(int(rng.integers(1, 5))):
+        pre = 16 * int(rng.integers(0, 41))
+        members = [pre + (0 if rng.random() < 0.2 else int(rng.integers(1, 700))) for _ in range(int(rng.integers(1, 9)))]
+        groups.append((pre, members))
+    singles = tuple(int(rng.choice([0, 1, 17, int(rng.integers(1, 900))])) for _ in range(int(rng.integers(0, 4))))
+    case_t = grouped_case(groups, H=H, D=D, B=B, dtype=dtype, seed=4000 + case, singles=singles)
+    q, kp, vp, tables, ctx, gs, gp = case_t
+    dev = torch.device("cuda")
+    S = q.shape[0]
+    mx = max(1, int(ctx.max()))
+    out = torch.full((S, H, D), float("nan"), dtype=TORCH_OUT[out_dtype], device=dev)
+    ws = pa.decode_grouped_workspace(S, H, D, mx, P, device=dev)
+    err = pa.new_error_flag(dev)
+    pa.pa_decode_grouped(out, q.to(dev), kp.to(dev), vp.to(dev), tables.to(dev), ctx.to(dev), mx, 1 / np.sqrt(D),
+                         gs.to(dev), gp.to(dev), ws, err, partition_size=P)
+    assert pa.pa_get_error(err) == 0, f"case {case}"
+    assert_attn_close(out, oracle_ref(case_t, dtype), out_dtype, f"grouped random case {case}")

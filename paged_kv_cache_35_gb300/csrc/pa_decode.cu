@@ -47,6 +47,13 @@
 //    planning runs and waits for it before reading anything.
 //  * pa_mixed_step (end of this file) puts the chunked prefill between the
 //    planning kernel and the decode kernel so that the two run concurrently.
+//  * pa_decode_grouped: for groups of sequences that share a prompt's blocks
+//    (parallel samples, beams), the planning kernel validates the groups and
+//    lists only each sequence's own tokens; the group kernel (tensor-core
+//    products of each tile with all of a group's queries) reads every shared
+//    prefix once and streams the listed items too (see the group kernel).
+//  * What the planning kernel writes (work list, counters, prefixes) is read
+//    by its dependents with coherent loads: they run while it writes.
 //  * Every wait is bounded; bad table entries are flagged, never trapped.
 #include <math.h>
 

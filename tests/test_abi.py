@@ -337,6 +337,29 @@ def test_prefix_groups_follow_the_tables(pa):
         pa.BlockAllocator(8, 16).prefix_groups([3])  # unknown sequence
 
 
+def test_prefix_groups_of_prefix_cached_requests(pa):
+    """Requests that reuse a cached prompt through the prefix cache hold its
+    blocks too: pa_alloc_prefix_groups groups them (8 at most) with the cached
+    prompt's full blocks as the prefix."""
+    B, L = 16, 1000
+    alloc = pa.BlockAllocator(2000, B, prefix_cache=True)
+    prompt = list(range(7, 7 + L))
+    assert alloc.add_seq_prefix(0, prompt) == 0  # empty cache: the first request appends its prompt
+    for t in prompt:
+        alloc.append_tokens([0], [t])
+    reused = []
+    for r in range(1, 11):
+        n0 = alloc.add_seq_prefix(r, prompt + [5000 + r])
+        reused.append(n0)
+        for t in (prompt + [5000 + r])[n0:]:
+            alloc.append_tokens([r], [t])
+    assert reused == [(L // B) * B] * 10  # every full prompt block is reused
+    starts, prefixes = alloc.prefix_groups(range(11))
+    assert starts.tolist() == [0, 8, 11]
+    assert prefixes.tolist() == [(L // B) * B] * 2
+    alloc.close()
+
+
 def test_grouped_workspace_sizes(pa):
     for S, H, D, mx in ((64, 40, 128, 1256), (4, 4, 64, 46), (256, 32, 128, 16384)):
         plain = pa.pa_decode_workspace_bytes(S, H, D, mx, 0)

@@ -339,23 +339,44 @@ __device__ __forceinline__ void consume_tile(const T* __restrict__ Ks, const T* 
 
 // Merge of all partitions of one (sequence, head) by one warp, in partition
 // order: M = max m_p, out = sum_p 2^(m_p - M) l_p o_p / sum_p 2^(m_p - M) l_p.
+// The partials are read kMergeBatch at a time (their loads in flight
+// together) and summed one by one in partition order, so the result does not
+// depend on the batching.
+constexpr int kMergeBatch = 4;
 template <int D>
 __device__ __forceinline__ void merge_partitions(const DecodeArgs& a, int s, int h, int nparts, int lane) {
   const size_t base = ((size_t)s * a.num_heads + h) * a.max_parts;
   float M = -INFINITY;
-  for (int p = 0; p < nparts; ++p) M = fmaxf(M, __ldcg(&a.part_ml[base + p].x));
+  for (int p0 = 0; p0 < nparts; p0 += kMergeBatch) {
+    float mp[kMergeBatch];
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) mp[i] = p0 + i < nparts ? __ldcg(&a.part_ml[base + p0 + i].x) : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) M = fmaxf(M, mp[i]);
+  }
   float L = 0.f;
   float O[D / 32];
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) O[i] = 0.f;
-  for (int p = 0; p < nparts; ++p) {
-    const float mp = __ldcg(&a.part_ml[base + p].x);
-    const float lp = __ldcg(&a.part_ml[base + p].y);
-    const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - M) * lp;
-    L += w;
-    const float* op = a.part_o + (base + p) * D;
+  for (int p0 = 0; p0 < nparts; p0 += kMergeBatch) {
+    float2 ml[kMergeBatch];
+    float ov[kMergeBatch][D / 32];
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) O[i] = fmaf(w, __ldcg(op + lane + 32 * i), O[i]);
+    for (int b = 0; b < kMergeBatch; ++b) {
+      const bool in = p0 + b < nparts;
+      ml[b] = in ? __ldcg(&a.part_ml[base + p0 + b]) : make_float2(-INFINITY, 0.f);
+      const float* op = a.part_o + (base + p0 + b) * D;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) ov[b][i] = in ? __ldcg(op + lane + 32 * i) : 0.f;
+    }
+#pragma unroll
+    for (int b = 0; b < kMergeBatch; ++b) {
+      if (p0 + b >= nparts) break;
+      const float w = (ml[b].x == -INFINITY) ? 0.f : exp2f(ml[b].x - M) * ml[b].y;
+      L += w;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) O[i] = fmaf(w, ov[b][i], O[i]);
+    }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const size_t ob = ((size_t)s * a.num_heads + h) * D;

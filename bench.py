@@ -486,6 +486,21 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+SPIN_CYCLES = 400_000  # ~0.2 ms at 2 GHz
+TIMING_NOTE = ("CUDA events around exactly K steps after a barrier and a synchronize; a ~0.2 ms GPU spin is "
+               "queued before the start event so that the host's enqueueing of the first step is not inside "
+               "the device-timed region; the clock samplers run from before the warm-up (no idle gap)")
+
+
+def spin_before_region():
+    """Keep the GPU busy while the host enqueues the start event and the
+    first steps: without it a short region (the driver's 20 steps) also
+    times the first launch's host latency, ~0.5 % per 20 steps."""
+    import torch
+
+    torch.cuda._sleep(SPIN_CYCLES)
+
+
 def time_calls(fn, stream, dev, n_back: int, n_each: int) -> dict:
     """Device time of one call of `fn` on `stream`: `n_back` calls back to
     back between two events (the mean, which the rooflines use), then
@@ -632,11 +647,14 @@ def measure_decode(args, rank, world, local, name, secondary=False):
         else:
             decode()
 
+    clocks = ClockSampler(local)
+    clocks.start()  # before the warm-up: the GPU stays busy up to the timed region
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
     flags = pa.pa_get_error(err, stream)
     if flags:
+        clocks.stop()
         raise RuntimeError(f"device error flags {flags} during warm-up")
 
     logical_bytes = decode_bytes(w.context_lens.tolist(), H, D, B, elt)
@@ -656,12 +674,10 @@ def measure_decode(args, rank, world, local, name, secondary=False):
 
     # ---- device-timed region: K steps back to back, nothing between them.
     t_start, t_end = ev(), ev()
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
     dist_barrier(world)
     torch.cuda.synchronize(dev)
     h0 = time.time()
+    spin_before_region()
     t_start.record(stream)
     for _ in range(K):
         step()
@@ -737,6 +753,7 @@ def measure_decode(args, rank, world, local, name, secondary=False):
         "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(name, w),
         "parallelism": f"replicas x{world}",
+        "timing": TIMING_NOTE,
         "seq_steps_per_s": seq_steps,
         "hbm_frac_of_measured_peak": value / world / peak,
         "hbm_frac_of_nominal_8tbs": value / world / 8000.0,
@@ -948,23 +965,24 @@ def measure_prefill(args, rank, world, local, name, secondary=False):
         pa.pa_reshape_and_cache(m.chunk_k, m.chunk_v, w.k_pool, w.v_pool, slots_d, err, stream)
         prefill()
 
+    clocks = ClockSampler(local)
+    clocks.start()  # before the warm-up: the GPU stays busy up to the timed region
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
     flags = pa.pa_get_error(err, stream)
     if flags:
+        clocks.stop()
         raise RuntimeError(f"device error flags {flags} during warm-up")
     flops = NP * 4 * D * H * L * (L + 1) // 2
 
     K = args.steps
     ev = lambda: torch.cuda.Event(enable_timing=True)
     t_start, t_end = ev(), ev()
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
     dist_barrier(world)
     torch.cuda.synchronize(dev)
     h0 = time.time()
+    spin_before_region()
     t_start.record(stream)
     for _ in range(K):
         step()
@@ -1002,6 +1020,7 @@ def measure_prefill(args, rank, world, local, name, secondary=False):
                    "l2": "no flush: inputs larger than L2 (per step the scatter reads 168 MB of new K/V and "
                          "writes it to the pool, the prefill reads it and 84 MB of queries and writes 84 MB)"},
         "parallelism": f"replicas x{world}",
+        "timing": TIMING_NOTE,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": pf_traffic, "peak_kind": peak_kind,
                      "kernel": "prefill_kernel (pa_prefill_chunk)", "algorithmic_flops_per_launch": flops,

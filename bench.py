@@ -856,6 +856,7 @@ def measure_decode(args, rank, world, local, name, secondary=False):
     torch.cuda.synchronize(dev)
     dist_barrier(world)
     e0, e1 = ev(), ev()
+    spin_before_region()
     e0.record(stream)
     s_in.wait_event(e0)
     for i in range(Ke):
@@ -1078,6 +1079,7 @@ def measure_prefill(args, rank, world, local, name, secondary=False):
     torch.cuda.synchronize(dev)
     dist_barrier(world)
     e0, e1 = ev(), ev()
+    spin_before_region()
     e0.record(stream)
     s_in.wait_event(e0)
     for i in range(Ke):

@@ -45,9 +45,9 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, from an ncu capture of one launch (dram__bytes_read.sum +
 # dram__bytes_write.sum); valid only for the decode kernel source whose
 # sha256 prefix is given (otherwise reported as null).
-TRAFFIC = {"bytes_per_launch": 1488291072, "kernel_sha256_prefix": "39c53e4475ea6ffd"}
+TRAFFIC = {"bytes_per_launch": 1488554240, "kernel_sha256_prefix": "60ec91adda895f35"}
 # The group kernel (pa_decode_grouped) on the parallel-sampling workload: DRAM bytes of one launch.
-GROUP_TRAFFIC = {"bytes_per_launch": 348377344, "kernel_sha256_prefix": "39c53e4475ea6ffd"}
+GROUP_TRAFFIC = {"bytes_per_launch": 348372736, "kernel_sha256_prefix": "60ec91adda895f35"}
 
 
 # DRAM bytes (read + write) per pa_prefill_chunk call on the four-prompt

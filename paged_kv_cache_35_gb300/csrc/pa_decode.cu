@@ -274,14 +274,58 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
   griddep_wait();
 }
 
+// Packed fp32 pairs: two independent IEEE fp32 operations per instruction
+// (round to nearest even, as the scalar forms).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// The 8 elements of a 16-byte vector as 4 fp32 pairs (elements 2i, 2i+1).
+template <typename T>
+__device__ __forceinline__ void to_pairs(const uint4& u, uint64_t* p);
+template <>
+__device__ __forceinline__ void to_pairs<__nv_bfloat16>(const uint4& u, uint64_t* p) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = f2_pack(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ void to_pairs<__half>(const uint4& u, uint64_t* p) {
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = __half22float2(h[i]);
+    p[i] = f2_pack(x.x, x.y);
+  }
+}
+
 // ---------------------------------------------------------------------------------
 // Consumer: one 16-token tile.  Lane (t4 = lane/8, c = lane%8) owns tokens
 // t4, t4+4, t4+8, t4+12 of the tile and the 16-byte vectors c (+8) of each
 // row: a group of 8 lanes reads one 128-byte stretch of a row, so the
-// shared-memory loads are conflict free.
+// shared-memory loads are conflict free.  The query, the output and each
+// row's elements are held as fp32 pairs (dimensions 2i, 2i+1); a score is the
+// sum of the even and the odd dimensions' dot products.
 template <int D, typename T>
 __device__ __forceinline__ void consume_tile(const T* __restrict__ Ks, const T* __restrict__ Vs, int nvalid,
-                                             const float* qf, float& m, float& l, float* o, int lane) {
+                                             const uint64_t* q2, float& m, float& l, uint64_t* o2, int lane) {
   constexpr int VPL = D / 64;
   const int t4 = lane >> 3;
   const int c = lane & 7;
@@ -290,15 +334,17 @@ __device__ __forceinline__ void consume_tile(const T* __restrict__ Ks, const T* 
   for (int i = 0; i < 4; ++i) {
     const int tok = t4 + 4 * i;
     const T* row = Ks + tok * D;
-    float acc = 0.f;
+    uint64_t acc2 = 0;  // (+0, +0)
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
       const uint4 u = *reinterpret_cast<const uint4*>(row + (c + 8 * v) * 8);
-      float f[8];
-      Elt<T>::to_float8(u, f);
+      uint64_t f[4];
+      to_pairs<T>(u, f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc = fmaf(qf[v * 8 + e], f[e], acc);
+      for (int e = 0; e < 4; ++e) acc2 = f2_fma(q2[v * 4 + e], f[e], acc2);
     }
+    const float2 ac = f2_unpack(acc2);
+    float acc = ac.x + ac.y;
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
@@ -317,20 +363,22 @@ __device__ __forceinline__ void consume_tile(const T* __restrict__ Ks, const T* 
     psum += pr[i];
   }
   l = l * alpha + psum;
+  const uint64_t alpha2 = f2_pack(alpha, alpha);
 #pragma unroll
-  for (int e = 0; e < 8 * VPL; ++e) o[e] *= alpha;
+  for (int e = 0; e < 4 * VPL; ++e) o2[e] = f2_mul(o2[e], alpha2);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int tok = t4 + 4 * i;
     if (tok < nvalid) {  // rows past the context may hold any bits (even NaN)
       const T* row = Vs + tok * D;
+      const uint64_t p2 = f2_pack(pr[i], pr[i]);
 #pragma unroll
       for (int v = 0; v < VPL; ++v) {
         const uint4 u = *reinterpret_cast<const uint4*>(row + (c + 8 * v) * 8);
-        float f[8];
-        Elt<T>::to_float8(u, f);
+        uint64_t f[4];
+        to_pairs<T>(u, f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[v * 8 + e] = fmaf(pr[i], f[e], o[v * 8 + e]);
+        for (int e = 0; e < 4; ++e) o2[v * 4 + e] = f2_fma(p2, f[e], o2[v * 4 + e]);
       }
     }
   }
@@ -576,21 +624,24 @@ __device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, 
     if (!__all_sync(0xffffffffu, ok)) break;
     const int4 un = sm.unit[qs];
     if (un.x < 0) break;
-    float qf[8 * VPL];
+    uint64_t q2[4 * VPL];
+    {
+      const uint64_t qs2 = f2_pack(a.qscale, a.qscale);
 #pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      const uint4 u = *reinterpret_cast<const uint4*>(&sm.qbuf[qs][(c + 8 * v) * 8]);
-      Elt<T>::to_float8(u, qf + 8 * v);
+      for (int v = 0; v < VPL; ++v) {
+        const uint4 u = *reinterpret_cast<const uint4*>(&sm.qbuf[qs][(c + 8 * v) * 8]);
+        to_pairs<T>(u, q2 + 4 * v);
+      }
+#pragma unroll
+      for (int e = 0; e < 4 * VPL; ++e) q2[e] = f2_mul(q2[e], qs2);
     }
-#pragma unroll
-    for (int e = 0; e < 8 * VPL; ++e) qf[e] *= a.qscale;
 
     const int ntok = un.w;
     const int nchunks = (ntok + kChunk - 1) / kChunk;
     float m = -INFINITY, l = 0.f;
-    float o[8 * VPL];
+    uint64_t o2[4 * VPL];
 #pragma unroll
-    for (int e = 0; e < 8 * VPL; ++e) o[e] = 0.f;
+    for (int e = 0; e < 4 * VPL; ++e) o2[e] = 0;  // (+0, +0)
     bool aborted = false;
     for (int j = warp; j < nchunks; j += kConsumerWarps, ++mine) {
       const int slot = warp * kSlotsPerWarp + (int)(mine % kSlotsPerWarp);
@@ -600,7 +651,7 @@ __device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, 
         break;
       }
       if (sm.slot_ok[slot]) {
-        consume_tile<D, T>(sm.ring[slot][0], sm.ring[slot][1], min(kChunk, ntok - j * kChunk), qf, m, l, o, lane);
+        consume_tile<D, T>(sm.ring[slot][0], sm.ring[slot][1], min(kChunk, ntok - j * kChunk), q2, m, l, o2, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
@@ -608,6 +659,13 @@ __device__ __forceinline__ void run_consumer(const DecodeArgs& a, DecodeSmem<D, 
     if (aborted) break;
 
     // merge the 4 token groups of the warp, leave the share for the merger
+    float o[8 * VPL];
+#pragma unroll
+    for (int e = 0; e < 4 * VPL; ++e) {
+      const float2 x = f2_unpack(o2[e]);
+      o[2 * e] = x.x;
+      o[2 * e + 1] = x.y;
+    }
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
 #pragma unroll

@@ -181,6 +181,12 @@ class NvmlPoller:
 
     def summary(self, t0, t1):
         inside = [(c, r) for t, c, r in self.samples if t0 <= t <= t1]
+        window = "timed region (NVML poll every 2 ms)"
+        if not inside:  # a region shorter than the poll period: the samples just before and after it
+            before = [(c, r) for t, c, r in self.samples if t < t0][-1:]
+            after = [(c, r) for t, c, r in self.samples if t > t1][:1]
+            inside = before + after
+            window = "the NVML samples just before and after the timed region (shorter than the 2 ms poll)"
         if not inside:
             return None
         names = {self.SW_POWER_CAP: "sw_power_cap", self.HW_SLOWDOWN: "hw_slowdown",
@@ -189,7 +195,7 @@ class NvmlPoller:
         reasons = sorted({n for c, r in inside for bit, n in names.items() if r & bit})
         mhz = [c for c, _ in inside]
         return {"sm_mhz": statistics.median(mhz), "sm_mhz_min": min(mhz), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(inside)}
+                "reasons": reasons, "samples": len(inside), "window": window}
 
 
 def _pci_bus_id(gpu_index: int):
@@ -224,6 +230,12 @@ class ClockSampler:
             self.proc = None
             return
         threading.Thread(target=self._read, daemon=True).start()
+        # nvidia-smi takes a moment to print its first line: wait for it (and
+        # for the first NVML sample) before the caller's warm-up, so that even
+        # a timed region of a fraction of a millisecond has samples around it
+        t_end = time.time() + 2.0
+        while time.time() < t_end and (not self.samples or (self.nvml.ok and not self.nvml.samples)):
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -267,7 +279,7 @@ class ClockSampler:
             res.update({"sm_mhz": fast["sm_mhz"], "sm_mhz_min": fast["sm_mhz_min"],
                         "sm_max_mhz": fast["sm_max_mhz"] or res.get("sm_max_mhz"),
                         "reasons": sorted(set(fast["reasons"]) | set(res.get("reasons", [])) - {"nvidia-smi unavailable"}),
-                        "samples": fast["samples"], "window": "timed region (NVML poll every 2 ms)"})
+                        "samples": fast["samples"], "window": fast["window"]})
         return res
 
 

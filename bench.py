@@ -510,7 +510,9 @@ def spin_before_region():
     times the first launch's host latency, ~0.5 % per 20 steps."""
     import torch
 
-    torch.cuda._sleep(SPIN_CYCLES)
+    spin = getattr(torch.cuda, "_sleep", None)
+    if spin is not None:
+        spin(SPIN_CYCLES)
 
 
 def time_calls(fn, stream, dev, n_back: int, n_each: int) -> dict:
